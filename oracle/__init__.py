@@ -1,0 +1,22 @@
+"""CPU oracle for DFlash-style block-diffusion drafting and greedy verification.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or run
+anything in this package.  The product (the CUDA library and its Python
+binding) never calls it and has no CPU fallback.
+
+Plain NumPy in float64, written from the method's description, sharing no code
+with the CUDA path (only the seeded generators in ``workload/`` feed both).
+
+Pins (tests/test_oracle_pins.py): every building block is checked against
+closed forms, textbook special cases, an independent library routine (PyTorch
+CPU ``rms_norm``, ``scaled_dot_product_attention``, ``linear``, ``silu``) or
+brute force; the composed draft step is pinned by invariants (non-causality,
+context-order invariance, RoPE shift invariance, incremental == one-shot
+context projection, DFlash-2 conv reductions) and the speculative loop by
+token identity with autoregressive greedy decoding.  Parity unpinned: the
+numerical values of a full random-init draft step have no external
+reference (there is no trained model and no printed example); only the
+pinned pieces and invariants above vouch for them.
+"""
+from .dflash_oracle import *  # noqa: F401,F403
