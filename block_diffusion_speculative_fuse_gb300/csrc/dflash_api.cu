@@ -1,0 +1,725 @@
+// C ABI: argument checks, TMA descriptors, workspace layout and the launch
+// sequences of the draft step, the context fuse / K-V injection, greedy
+// verify and the causal target forward.  Host code only; every arithmetic
+// step runs in the kernels of this library.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/dflash.h"
+#include "kernels.h"
+
+using namespace dflash;
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda = static_cast<int>(e);
+  return DFLASH_ERR_CUDA;
+}
+#define DF_CUDA(expr)                               \
+  do {                                              \
+    cudaError_t e__ = (expr);                       \
+    if (e__ != cudaSuccess) return cuda_fail(e__);  \
+  } while (0)
+
+// ---------------------------------------------------------------- driver entry
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int load_encode() {
+  if (g_encode != nullptr) return DFLASH_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return DFLASH_ERR_NO_DEVICE;
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return DFLASH_OK;
+}
+
+// 2-D bf16 map over [rows][cols] (row stride ld elements), box [box_rows][64],
+// 128-byte swizzle, zero fill out of bounds.
+int encode_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+               uint32_t box_rows) {
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (ld * 2) % 16 != 0)
+    return DFLASH_ERR_INVALID_ARG;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ERR_INVALID_ARG;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+struct dflash_model_s {
+  dflash_config cfg;
+  dflash_weights w;
+  int device = 0;
+  int sms = 148;
+  bool is_draft = false;
+  CUtensorMap m_wqkv, m_wo, m_gu, m_down, m_lm, m_fc;
+  float2 rope[kMaxRopePairs];
+  int qkv_rows = 0, q_dim = 0, kv_dim = 0;
+};
+
+namespace {
+
+constexpr size_t kHeaderBytes = 64 * 1024;       // status word + split counters
+constexpr int kMaxCounters = (kHeaderBytes - 256) / 4;
+constexpr int kTargetSplitKeys = 512;
+
+size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+const uint16_t* u16(const void* p) { return static_cast<const uint16_t*>(p); }
+
+// Split-K count: enough CTAs for one resident wave, at least 2 k-blocks per
+// split.  For a target (batch-invariant path) it depends on the weight shape
+// only, never on the number of activation rows.
+int choose_splits(const dflash_model_s* m, int n_tiles, int m_tiles, int kb_total, int bn) {
+  const int per_sm = bn <= 64 ? 2 : 1;
+  const int capacity = m->sms * (m->is_draft ? per_sm : 2);
+  const int base = n_tiles * (m->is_draft ? m_tiles : 1);
+  int s = capacity / std::max(1, base);
+  s = std::max(1, std::min(s, kb_total / 2));
+  s = std::min(s, 32);
+  return s;
+}
+
+struct Ws {
+  uint8_t* base = nullptr;
+  size_t off = kHeaderBytes;
+  size_t cap = 0;
+  bool dry = false;
+  template <typename T>
+  T* take(size_t n) {
+    T* p = dry ? nullptr : reinterpret_cast<T*>(base + off);
+    off = al256(off + n * sizeof(T));
+    return p;
+  }
+  int32_t* status() const { return dry ? nullptr : reinterpret_cast<int32_t*>(base); }
+  int32_t* counters() const { return dry ? nullptr : reinterpret_cast<int32_t*>(base + 256); }
+};
+
+// Buffers of one stack pass over `rows` activation rows (+ ctx rows on the QKV input).
+struct StackBufs {
+  float* x;
+  uint16_t* a;     // [rows + ctx][H]
+  uint16_t* q;     // [rows][hq][d]
+  uint16_t* kblk;
+  uint16_t* vblk;
+  float* o_part;
+  float* ml_part;
+  uint16_t* o;     // [rows][q_dim]
+  uint16_t* a2;    // [rows][H]
+  uint16_t* hmid;  // [rows][F]
+  float* partial;
+  float* amax_val;
+  int32_t* amax_idx;
+  float* ctx_f32;
+};
+
+struct GemmShape {
+  int N, K, m_rows;
+};
+
+size_t partial_floats(const dflash_model_s* m, int rows_main, int rows_qkv) {
+  const dflash_config& c = m->cfg;
+  const GemmShape shapes[6] = {{m->qkv_rows, c.hidden, rows_qkv},
+                               {2 * m->kv_dim, c.hidden, rows_qkv},
+                               {c.hidden, m->q_dim, rows_main},
+                               {2 * c.mlp, c.hidden, rows_main},
+                               {c.hidden, c.mlp, rows_main},
+                               {c.hidden, c.n_taps * c.hidden, rows_qkv}};
+  size_t mx = 0;
+  for (const GemmShape& g : shapes) {
+    if (g.K <= 0 || g.N <= 0 || g.m_rows <= 0) continue;
+    const int bn = gemm_bn_for(g.m_rows);
+    const int mt = (g.m_rows + bn - 1) / bn;
+    const int s = choose_splits(m, g.N / kTileN, mt, g.K / kTileK, bn);
+    if (s > 1) mx = std::max(mx, static_cast<size_t>(s) * g.m_rows * g.N);
+  }
+  return mx;
+}
+
+int attn_split_keys(const dflash_model_s* m, int batch, int max_keys) {
+  if (!m->is_draft) return kTargetSplitKeys;
+  const long long work = static_cast<long long>(max_keys) * batch * m->cfg.n_kv_heads;
+  long long s = (work + 2LL * m->sms - 1) / (2LL * m->sms);
+  s = ((s + 63) / 64) * 64;
+  s = std::max<long long>(128, std::min<long long>(2048, s));
+  return static_cast<int>(s);
+}
+int attn_n_splits(const dflash_model_s* m, int split_keys, int max_keys) {
+  const int n = (max_keys + split_keys - 1) / split_keys;
+  return m->is_draft ? n + 1 : std::max(1, n);
+}
+
+void layout_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n, int ctx_rows,
+                  int max_keys) {
+  const dflash_config& c = m->cfg;
+  const int rows = batch * n;
+  b.x = ws.take<float>(static_cast<size_t>(rows) * c.hidden);
+  b.a = ws.take<uint16_t>(static_cast<size_t>(rows + ctx_rows) * c.hidden);
+  b.q = ws.take<uint16_t>(static_cast<size_t>(rows) * m->q_dim);
+  b.kblk = ws.take<uint16_t>(static_cast<size_t>(rows) * m->kv_dim);
+  b.vblk = ws.take<uint16_t>(static_cast<size_t>(rows) * m->kv_dim);
+  const int sk = attn_split_keys(m, batch, max_keys);
+  const int ns = attn_n_splits(m, sk, max_keys);
+  b.o_part = ws.take<float>(static_cast<size_t>(ns) * rows * c.n_q_heads * c.head_dim);
+  b.ml_part = ws.take<float>(static_cast<size_t>(ns) * rows * c.n_q_heads * 2);
+  b.o = ws.take<uint16_t>(static_cast<size_t>(rows) * m->q_dim);
+  b.a2 = ws.take<uint16_t>(static_cast<size_t>(rows) * c.hidden);
+  b.hmid = ws.take<uint16_t>(static_cast<size_t>(rows) * c.mlp);
+  b.partial = ws.take<float>(partial_floats(m, rows, rows + ctx_rows));
+  const int vt = c.vocab / kTileN;
+  b.amax_val = ws.take<float>(static_cast<size_t>(rows) * vt);
+  b.amax_idx = ws.take<int32_t>(static_cast<size_t>(rows) * vt);
+  b.ctx_f32 = nullptr;
+}
+
+GemmParams gemm_base(const dflash_model_s* m, int M, int N, int K, int bn, Ws& ws) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.w_tile_step = kTileN;
+  p.w_half_gap = 64;
+  p.kb_total = K / kTileK;
+  const int mt = (M + bn - 1) / bn;
+  p.splits = choose_splits(m, N / kTileN, mt, p.kb_total, bn);
+  p.kb_per_split = (p.kb_total + p.splits - 1) / p.splits;
+  p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;
+  p.counters = ws.counters();
+  p.status = ws.status();
+  return p;
+}
+
+int run_gemm(const dflash_model_s* m, const CUtensorMap* wmap, const void* x, int ld_x,
+             GemmParams& p, float* partial, cudaStream_t s) {
+  const int bn = gemm_bn_for(p.M);
+  const int mt = (p.M + bn - 1) / bn;
+  if (p.splits > 1) {
+    if ((p.N / kTileN) * mt > kMaxCounters) return DFLASH_ERR_CAPACITY;
+    p.partial = partial;
+  }
+  CUtensorMap xmap;
+  int rc = encode_map(&xmap, x, p.M, p.K, ld_x, bn);
+  if (rc) return rc;
+  DF_CUDA(gemm_launch(wmap, &xmap, p, bn, s, true));
+  return DFLASH_OK;
+}
+
+QkvEpi qkv_base(const dflash_model_s* m, int layer) {
+  const dflash_config& c = m->cfg;
+  QkvEpi e;
+  std::memset(&e, 0, sizeof(e));
+  e.n_q_heads = c.n_q_heads;
+  e.n_kv_heads = c.n_kv_heads;
+  e.head_dim = c.head_dim;
+  e.eps = c.rms_eps;
+  if (c.qk_norm) {
+    e.q_norm = u16(m->w.q_norm) + static_cast<size_t>(layer) * c.head_dim;
+    e.k_norm = u16(m->w.k_norm) + static_cast<size_t>(layer) * c.head_dim;
+  }
+  e.page_size = c.page_size;
+  std::memcpy(e.rope, m->rope, sizeof(e.rope));
+  return e;
+}
+
+size_t layer_pool_elems(const dflash_model_s* m, const dflash_kv* kv) {
+  return static_cast<size_t>(kv->n_pages) * 2 * m->cfg.n_kv_heads * m->cfg.page_size *
+         m->cfg.head_dim;
+}
+
+void set_pool(const dflash_model_s* m, QkvEpi& e, const dflash_kv* kv, int layer) {
+  e.pool = static_cast<uint16_t*>(kv->pool) + layer_pool_elems(m, kv) * layer;
+  e.page_table = kv->page_table;
+  e.max_pages = kv->max_pages;
+  e.n_pages = kv->n_pages;
+}
+
+int check_kv(const dflash_model_s* m, const dflash_kv* kv) {
+  if (kv == nullptr || kv->pool == nullptr || kv->page_table == nullptr || kv->n_pages <= 0 ||
+      kv->max_pages <= 0)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(kv->pool)) return DFLASH_ERR_INVALID_ARG;
+  (void)m;
+  return DFLASH_OK;
+}
+
+// One decoder-layer stack pass (embedding already done: b.x / b.a filled).
+// draft: block rows (non-causal, block K/V), else target rows (causal).
+int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
+              const int32_t* pos0, const dflash_kv* kv, int ctx_rows, const int32_t* ctx_req,
+              const int32_t* ctx_pos, const int32_t* tap_slot, int n_taps, uint16_t* taps,
+              cudaStream_t s) {
+  const dflash_config& c = m->cfg;
+  const int rows = batch * n;
+  const int H = c.hidden;
+  const int max_keys = kv->max_pages * c.page_size;
+  for (int l = 0; l < c.n_layers; ++l) {
+    if (l > 0) {
+      uint16_t* raw = nullptr;
+      if (taps != nullptr && tap_slot[l - 1] >= 0) raw = taps + static_cast<size_t>(tap_slot[l - 1]) * H;
+      DF_CUDA(rmsnorm_launch(b.x, rows, H, u16(m->w.in_norm) + static_cast<size_t>(l) * H,
+                             c.rms_eps, b.a, H, raw, n_taps * H, s, true));
+    }
+    // QKV (+ context K/V rows in the same weight pass)
+    {
+      const int M = rows + ctx_rows;
+      GemmParams p = gemm_base(m, M, m->qkv_rows, H, gemm_bn_for(M), ws);
+      p.w_row0 = l * m->qkv_rows;
+      p.mode = EPI_QKV;
+      QkvEpi e = qkv_base(m, l);
+      set_pool(m, e, kv, l);
+      e.q = b.q;
+      if (m->is_draft) {
+        e.n_blk = rows;
+        e.block = n;
+        e.anchor_pos = pos0;
+        e.pool_req = ctx_req;
+        e.pool_pos = ctx_pos;
+        e.keep_q_pool = 0;
+        e.kblk = b.kblk;
+        e.vblk = b.vblk;
+      } else {
+        e.n_blk = 0;
+        e.rows_per_req = n;
+        e.pool_pos0 = pos0;
+        e.keep_q_pool = 1;
+      }
+      p.qkv = e;
+      int rc = run_gemm(m, &m->m_wqkv, b.a, H, p, b.partial, s);
+      if (rc) return rc;
+    }
+    // attention
+    {
+      AttnParams a;
+      std::memset(&a, 0, sizeof(a));
+      a.q = b.q;
+      a.batch = batch;
+      a.n = n;
+      a.pos0 = pos0;
+      a.causal = m->is_draft ? 0 : 1;
+      a.pool = static_cast<const uint16_t*>(kv->pool) + layer_pool_elems(m, kv) * l;
+      a.page_table = kv->page_table;
+      a.max_pages = kv->max_pages;
+      a.n_pages = kv->n_pages;
+      a.page_size = c.page_size;
+      a.kblk = b.kblk;
+      a.vblk = b.vblk;
+      a.hq = c.n_q_heads;
+      a.hkv = c.n_kv_heads;
+      a.d = c.head_dim;
+      a.split_keys = attn_split_keys(m, batch, max_keys);
+      a.n_splits = attn_n_splits(m, a.split_keys, max_keys);
+      a.o_part = b.o_part;
+      a.ml_part = b.ml_part;
+      a.out = b.o;
+      a.status = ws.status();
+      DF_CUDA(attention_launch(a, s, true));
+    }
+    // O projection + residual (+ DFlash-2 block conv)
+    {
+      GemmParams p = gemm_base(m, rows, H, m->q_dim, gemm_bn_for(rows), ws);
+      p.w_row0 = l * H;
+      p.mode = EPI_RESID;
+      p.resid = b.x;
+      p.ld_resid = H;
+      if (m->is_draft && c.conv_width > 0 && m->w.conv != nullptr) {
+        p.conv = u16(m->w.conv) + static_cast<size_t>(l) * H * c.conv_width;
+        p.conv_width = c.conv_width;
+        p.block = n;
+      }
+      int rc = run_gemm(m, &m->m_wo, b.o, m->q_dim, p, b.partial, s);
+      if (rc) return rc;
+    }
+    DF_CUDA(rmsnorm_launch(b.x, rows, H, u16(m->w.post_norm) + static_cast<size_t>(l) * H,
+                           c.rms_eps, b.a2, H, nullptr, 0, s, true));
+    // gate/up + SwiGLU: each 128-row tile = 64 gate rows + the matching 64 up rows
+    {
+      GemmParams p = gemm_base(m, rows, 2 * c.mlp, H, gemm_bn_for(rows), ws);
+      p.w_row0 = l * 2 * c.mlp;
+      p.w_tile_step = 64;
+      p.w_half_gap = c.mlp;
+      p.mode = EPI_SWIGLU;
+      p.out = b.hmid;
+      p.ld_out = c.mlp;
+      int rc = run_gemm(m, &m->m_gu, b.a2, H, p, b.partial, s);
+      if (rc) return rc;
+    }
+    // down projection + residual
+    {
+      GemmParams p = gemm_base(m, rows, H, c.mlp, gemm_bn_for(rows), ws);
+      p.w_row0 = l * H;
+      p.mode = EPI_RESID;
+      p.resid = b.x;
+      p.ld_resid = H;
+      int rc = run_gemm(m, &m->m_down, b.hmid, c.mlp, p, b.partial, s);
+      if (rc) return rc;
+    }
+  }
+  // final norm (+ tap of the last layer)
+  uint16_t* raw = nullptr;
+  if (taps != nullptr && tap_slot[c.n_layers - 1] >= 0)
+    raw = taps + static_cast<size_t>(tap_slot[c.n_layers - 1]) * H;
+  DF_CUDA(rmsnorm_launch(b.x, rows, H, u16(m->w.final_norm), c.rms_eps, b.a2, H, raw, n_taps * H,
+                         s, true));
+  return DFLASH_OK;
+}
+
+int run_lm_head(const dflash_model_s* m, Ws& ws, StackBufs& b, int rows, int block,
+                int skip_first, int32_t* out, float* logits, cudaStream_t s) {
+  const dflash_config& c = m->cfg;
+  GemmParams p = gemm_base(m, rows, c.vocab, c.hidden, gemm_bn_for(rows), ws);
+  p.mode = EPI_ARGMAX;
+  p.amax_val = b.amax_val;
+  p.amax_idx = b.amax_idx;
+  p.logits = logits;
+  p.ld_logits = c.vocab;
+  p.splits = 1;  // argmax needs the full dot product per tile
+  p.kb_per_split = p.kb_total;
+  int rc = run_gemm(m, &m->m_lm, b.a2, c.hidden, p, b.partial, s);
+  if (rc) return rc;
+  DF_CUDA(argmax_reduce_launch(b.amax_val, b.amax_idx, rows, c.vocab / kTileN, block, out,
+                               skip_first, s, true));
+  return DFLASH_OK;
+}
+
+int check_cfg(const dflash_config* c, bool draft) {
+  if (c->n_layers < 1 || c->hidden < 128 || c->hidden % 128 || c->vocab < 128 || c->vocab % 128)
+    return DFLASH_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return DFLASH_ERR_UNSUPPORTED;
+  if (c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads) return DFLASH_ERR_UNSUPPORTED;
+  const int g = c->n_q_heads / c->n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return DFLASH_ERR_UNSUPPORTED;
+  if (((c->n_q_heads + 2 * c->n_kv_heads) * c->head_dim) % 128) return DFLASH_ERR_UNSUPPORTED;
+  if ((c->n_q_heads * c->head_dim) % 64 || c->mlp < 64 || c->mlp % 64) return DFLASH_ERR_UNSUPPORTED;
+  if (c->page_size != 16) return DFLASH_ERR_UNSUPPORTED;
+  if (draft) {
+    if (c->block < 1 || c->block > 32 || 256 % c->block) return DFLASH_ERR_UNSUPPORTED;
+    if (c->n_taps < 1) return DFLASH_ERR_UNSUPPORTED;
+    if (c->conv_width < 0 || c->conv_width > 7 || (c->conv_width && c->conv_width % 2 == 0))
+      return DFLASH_ERR_UNSUPPORTED;
+  }
+  if (!(c->rms_eps >= 0.f) || !(c->rope_base > 1.f)) return DFLASH_ERR_INVALID_ARG;
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+// ======================================================================= ABI
+extern "C" {
+
+const char* dflash_strerror(int code) {
+  switch (code) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_UNSUPPORTED: return "unsupported shape";
+    case DFLASH_ERR_CAPACITY: return "capacity exceeded (workspace, page table or cache)";
+    case DFLASH_ERR_CUDA: return "CUDA error";
+    case DFLASH_ERR_TIMEOUT: return "device wait timed out";
+    case DFLASH_ERR_NO_DEVICE: return "no compute-capability 10.3 device or driver entry point";
+    default: return "unknown error";
+  }
+}
+
+int dflash_last_cuda_error(void) { return g_last_cuda; }
+
+int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflash_model* out) {
+  if (cfg == nullptr || w == nullptr || out == nullptr) return DFLASH_ERR_INVALID_ARG;
+  *out = nullptr;
+  const bool draft = cfg->block > 0;
+  int rc = check_cfg(cfg, draft);
+  if (rc) return rc;
+  const void* need[] = {w->embed, w->lm_head, w->final_norm, w->in_norm, w->wqkv, w->wo,
+                        w->post_norm, w->w_gate_up, w->w_down};
+  for (const void* p : need)
+    if (p == nullptr || !aligned16(p)) return DFLASH_ERR_INVALID_ARG;
+  if (cfg->qk_norm && (w->q_norm == nullptr || w->k_norm == nullptr)) return DFLASH_ERR_INVALID_ARG;
+  if (draft && (w->fc == nullptr || w->mask_embed == nullptr || !aligned16(w->fc) ||
+                (cfg->fc_norm && w->fc_norm == nullptr)))
+    return DFLASH_ERR_INVALID_ARG;
+  if (draft && cfg->conv_width > 0 && w->conv == nullptr) return DFLASH_ERR_INVALID_ARG;
+
+  int dev = 0;
+  DF_CUDA(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  DF_CUDA(cudaGetDeviceProperties(&prop, dev));
+  if (prop.major != 10 || prop.minor != 3) return DFLASH_ERR_NO_DEVICE;
+  rc = load_encode();
+  if (rc) return rc;
+
+  dflash_model_s* m = new (std::nothrow) dflash_model_s();
+  if (m == nullptr) return DFLASH_ERR_CAPACITY;
+  m->cfg = *cfg;
+  m->w = *w;
+  m->device = dev;
+  m->sms = prop.multiProcessorCount;
+  m->is_draft = draft;
+  m->q_dim = cfg->n_q_heads * cfg->head_dim;
+  m->kv_dim = cfg->n_kv_heads * cfg->head_dim;
+  m->qkv_rows = m->q_dim + 2 * m->kv_dim;
+  const uint64_t L = cfg->n_layers, H = cfg->hidden, F = cfg->mlp;
+  rc = encode_map(&m->m_wqkv, w->wqkv, L * m->qkv_rows, H, H, 64);
+  if (!rc) rc = encode_map(&m->m_wo, w->wo, L * H, m->q_dim, m->q_dim, 64);
+  if (!rc) rc = encode_map(&m->m_gu, w->w_gate_up, L * 2 * F, H, H, 64);
+  if (!rc) rc = encode_map(&m->m_down, w->w_down, L * H, F, F, 64);
+  if (!rc) rc = encode_map(&m->m_lm, w->lm_head, cfg->vocab, H, H, 64);
+  if (!rc && draft)
+    rc = encode_map(&m->m_fc, w->fc, H, static_cast<uint64_t>(cfg->n_taps) * H,
+                    static_cast<uint64_t>(cfg->n_taps) * H, 64);
+  if (rc) {
+    delete m;
+    return rc;
+  }
+  // inv_freq_p = base^(-2p/d) as an unevaluated (hi, lo) float pair
+  const int half = cfg->head_dim / 2;
+  for (int p = 0; p < kMaxRopePairs; ++p) {
+    double f = p < half ? std::pow(static_cast<double>(cfg->rope_base),
+                                   -2.0 * p / static_cast<double>(cfg->head_dim))
+                        : 0.0;
+    const float hi = static_cast<float>(f);
+    m->rope[p] = make_float2(hi, static_cast<float>(f - static_cast<double>(hi)));
+  }
+  *out = m;
+  return DFLASH_OK;
+}
+
+int dflash_model_destroy(dflash_model m) {
+  delete m;
+  return DFLASH_OK;
+}
+
+size_t dflash_workspace_bytes(dflash_model m, int32_t max_block_rows, int32_t max_ctx_rows,
+                              int32_t max_batch, int32_t max_ctx_len) {
+  if (m == nullptr || max_block_rows < 0 || max_ctx_rows < 0 || max_batch < 1 || max_ctx_len < 0)
+    return 0;
+  const dflash_config& c = m->cfg;
+  const int max_keys = ((max_ctx_len + c.page_size - 1) / c.page_size) * c.page_size;
+  size_t need = kHeaderBytes;
+  // stack pass (draft block or target rows); block rows are batch*B, split across
+  // the batch as n = rows / batch
+  if (max_block_rows > 0) {
+    Ws ws;
+    ws.dry = true;
+    StackBufs b;
+    const int n = std::max(1, max_block_rows / max_batch);
+    layout_stack(m, ws, b, max_batch, n, max_ctx_rows, max_keys);
+    // the attention partials are sized for the worst split count over batch sizes
+    for (int bt = 1; bt <= max_batch; bt *= 2) {
+      Ws w2;
+      w2.dry = true;
+      StackBufs b2;
+      layout_stack(m, w2, b2, bt, std::max(1, max_block_rows / bt), max_ctx_rows, max_keys);
+      need = std::max(need, w2.off);
+    }
+    need = std::max(need, ws.off);
+  }
+  if (max_ctx_rows > 0 && m->is_draft) {
+    Ws ws;
+    ws.dry = true;
+    ws.take<float>(partial_floats(m, 0, max_ctx_rows));
+    ws.take<float>(static_cast<size_t>(max_ctx_rows) * c.hidden);
+    need = std::max(need, ws.off);
+  }
+  return need;
+}
+
+int dflash_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr || ws_bytes < kHeaderBytes || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return DFLASH_ERR_INVALID_ARG;
+  DF_CUDA(cudaMemsetAsync(ws, 0, kHeaderBytes, static_cast<cudaStream_t>(stream)));
+  return DFLASH_OK;
+}
+
+int dflash_get_status(const void* ws, int32_t* status, int32_t* site, void* stream) {
+  if (ws == nullptr || status == nullptr) return DFLASH_ERR_INVALID_ARG;
+  int32_t h[2] = {0, 0};
+  DF_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  DF_CUDA(cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost));
+  *status = h[0];
+  if (site) *site = h[1];
+  return DFLASH_OK;
+}
+
+int dflash_ctx_fuse(dflash_model m, const void* taps, int32_t T, void* ctx, void* ws,
+                    size_t ws_bytes, void* stream) {
+  if (m == nullptr || !m->is_draft || taps == nullptr || ctx == nullptr || ws == nullptr || T < 1)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(taps) || !aligned16(ctx) || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = m->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Ws w;
+  w.base = static_cast<uint8_t*>(ws);
+  float* partial = w.take<float>(partial_floats(m, 0, T));
+  float* cf = w.take<float>(static_cast<size_t>(T) * c.hidden);
+  if (w.off > ws_bytes) return DFLASH_ERR_CAPACITY;
+  const int K = c.n_taps * c.hidden;
+  GemmParams p = gemm_base(m, T, c.hidden, K, gemm_bn_for(T), w);
+  if (c.fc_norm) {
+    p.mode = EPI_STORE_F32;
+    p.out = cf;
+  } else {
+    p.mode = EPI_STORE_BF16;
+    p.out = ctx;
+  }
+  p.ld_out = c.hidden;
+  int rc = run_gemm(m, &m->m_fc, taps, K, p, partial, s);
+  if (rc) return rc;
+  if (c.fc_norm)
+    DF_CUDA(rmsnorm_launch(cf, T, c.hidden, u16(m->w.fc_norm), c.rms_eps,
+                           static_cast<uint16_t*>(ctx), c.hidden, nullptr, 0, s, true));
+  return DFLASH_OK;
+}
+
+int dflash_kv_append(dflash_model m, const void* ctx, const int32_t* row_req,
+                     const int32_t* row_pos, int32_t T, const dflash_kv* kv, void* ws,
+                     size_t ws_bytes, void* stream) {
+  if (m == nullptr || ctx == nullptr || row_req == nullptr || row_pos == nullptr || T < 1 ||
+      ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || !aligned16(ctx))
+    return DFLASH_ERR_INVALID_ARG;
+  int rc = check_kv(m, kv);
+  if (rc) return rc;
+  const dflash_config& c = m->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Ws w;
+  w.base = static_cast<uint8_t*>(ws);
+  float* partial = w.take<float>(partial_floats(m, 0, T));
+  if (w.off > ws_bytes) return DFLASH_ERR_CAPACITY;
+  for (int l = 0; l < c.n_layers; ++l) {
+    GemmParams p = gemm_base(m, T, 2 * m->kv_dim, c.hidden, gemm_bn_for(T), w);
+    p.w_row0 = l * m->qkv_rows + m->q_dim;
+    p.mode = EPI_QKV;
+    QkvEpi e = qkv_base(m, l);
+    set_pool(m, e, kv, l);
+    e.n_blk = 0;
+    e.pool_req = row_req;
+    e.pool_pos = row_pos;
+    e.keep_q_pool = 0;
+    e.f0 = m->q_dim;
+    p.qkv = e;
+    rc = run_gemm(m, &m->m_wqkv, ctx, c.hidden, p, partial, s);
+    if (rc) return rc;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(dflash_model m, const int32_t* anchor, const int32_t* anchor_pos,
+                       int32_t batch, const dflash_kv* kv, const void* pending_ctx,
+                       const int32_t* pending_req, const int32_t* pending_pos, int32_t T,
+                       int32_t* draft, float* logits, float* hidden, void* ws, size_t ws_bytes,
+                       void* stream) {
+  if (m == nullptr || !m->is_draft || anchor == nullptr || anchor_pos == nullptr || batch < 1 ||
+      draft == nullptr || ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || T < 0)
+    return DFLASH_ERR_INVALID_ARG;
+  if (T > 0 && (pending_ctx == nullptr || pending_req == nullptr || pending_pos == nullptr ||
+                !aligned16(pending_ctx)))
+    return DFLASH_ERR_INVALID_ARG;
+  int rc = check_kv(m, kv);
+  if (rc) return rc;
+  const dflash_config& c = m->cfg;
+  const int B = c.block;
+  const int rows = batch * B;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Ws w;
+  w.base = static_cast<uint8_t*>(ws);
+  StackBufs b;
+  const int max_keys = kv->max_pages * c.page_size;
+  layout_stack(m, w, b, batch, B, T, max_keys);
+  if (w.off > ws_bytes) return DFLASH_ERR_CAPACITY;
+  DF_CUDA(embed_block_launch(anchor, batch, B, u16(m->w.embed), u16(m->w.mask_embed),
+                             u16(m->w.in_norm), c.rms_eps, c.hidden, b.x, b.a, c.hidden,
+                             u16(pending_ctx), T, s, true, w.status(), c.vocab));
+  rc = run_stack(m, w, b, batch, B, anchor_pos, kv, T, pending_req, pending_pos, nullptr, 0,
+                 nullptr, s);
+  if (rc) return rc;
+  if (B > 1 || logits != nullptr) {
+    rc = run_lm_head(m, w, b, rows, B, 1, draft, logits, s);
+    if (rc) return rc;
+  }
+  if (hidden != nullptr)
+    DF_CUDA(copy_rows_f32_launch(b.x, hidden, static_cast<size_t>(rows) * c.hidden, s, true));
+  return DFLASH_OK;
+}
+
+int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t batch, int32_t B,
+                         int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
+                         int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
+                         const int32_t* anchor_pos_in, int32_t* anchor_pos_out, void* stream) {
+  if (target == nullptr || batch < 1 || B < 1 || B > 32 || (B > 1 && draft == nullptr))
+    return DFLASH_ERR_INVALID_ARG;
+  if ((tgt_len_out != nullptr && tgt_len_in == nullptr) ||
+      (anchor_pos_out != nullptr && anchor_pos_in == nullptr))
+    return DFLASH_ERR_INVALID_ARG;
+  DF_CUDA(verify_launch(draft, target, batch, B, out_tokens, n_accept, tgt_len_in, tgt_len_out,
+                        ctx_pending, anchor_out, anchor_pos_in, anchor_pos_out,
+                        static_cast<cudaStream_t>(stream), true));
+  return DFLASH_OK;
+}
+
+int dflash_target_forward(dflash_model m, const int32_t* tokens, const int32_t* pos0,
+                          int32_t batch, int32_t n, const dflash_kv* kv,
+                          const int32_t* tap_layers, int32_t n_taps, void* taps,
+                          int32_t* argmax, float* logits, void* ws, size_t ws_bytes,
+                          void* stream) {
+  if (m == nullptr || m->is_draft || tokens == nullptr || pos0 == nullptr || batch < 1 || n < 1 ||
+      argmax == nullptr || ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return DFLASH_ERR_INVALID_ARG;
+  if (n_taps < 0 || (n_taps > 0 && (tap_layers == nullptr || taps == nullptr)))
+    return DFLASH_ERR_INVALID_ARG;
+  int rc = check_kv(m, kv);
+  if (rc) return rc;
+  const dflash_config& c = m->cfg;
+  std::vector<int32_t> slot(c.n_layers, -1);
+  for (int i = 0; i < n_taps; ++i) {
+    if (tap_layers[i] < 0 || tap_layers[i] >= c.n_layers || slot[tap_layers[i]] >= 0)
+      return DFLASH_ERR_INVALID_ARG;
+    slot[tap_layers[i]] = i;
+  }
+  const int rows = batch * n;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Ws w;
+  w.base = static_cast<uint8_t*>(ws);
+  StackBufs b;
+  layout_stack(m, w, b, batch, n, 0, kv->max_pages * c.page_size);
+  if (w.off > ws_bytes) return DFLASH_ERR_CAPACITY;
+  DF_CUDA(embed_tokens_launch(tokens, rows, u16(m->w.embed), u16(m->w.in_norm), c.rms_eps,
+                              c.hidden, b.x, b.a, s, true, w.status(), c.vocab));
+  rc = run_stack(m, w, b, batch, n, pos0, kv, 0, nullptr, nullptr, slot.data(), n_taps,
+                 static_cast<uint16_t*>(taps), s);
+  if (rc) return rc;
+  return run_lm_head(m, w, b, rows, n, 0, argmax, logits, s);
+}
+
+int dflash_synth_target(const int32_t* draft, int32_t batch, int32_t B, const uint64_t* threshold,
+                        int32_t vocab, uint64_t seed, int64_t* step, int32_t advance,
+                        int32_t* target, void* stream) {
+  if (threshold == nullptr || step == nullptr || target == nullptr || batch < 1 || B < 1 ||
+      vocab < 2 || batch * B > 1024 || (B > 1 && draft == nullptr))
+    return DFLASH_ERR_INVALID_ARG;
+  DF_CUDA(synth_target_launch(draft, batch, B, threshold, vocab, seed, step, advance, target,
+                              static_cast<cudaStream_t>(stream), true));
+  return DFLASH_OK;
+}
+
+}  // extern "C"

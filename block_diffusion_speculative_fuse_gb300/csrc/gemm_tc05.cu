@@ -1,0 +1,485 @@
+// Weight-streaming GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+//   Y[m][n] = sum_k X[m][k] * W[n][k]        (y = x W^T, W stored [out][in])
+//
+// "Swap-AB" orientation: 128 weight rows form the MMA M side, the (few)
+// activation rows the MMA N side (BN = 16..256), so a decode-sized batch
+// still fills the 128-lane tensor core and the kernel streams W at HBM speed.
+//
+// Per CTA (128 threads): one 128-row weight tile x one BN-row activation tile
+// over a K range (split-K).  Warp 0 lane 0 issues TMA loads into a STAGES-deep
+// shared-memory ring (128-byte swizzle, 64 K-elements per stage); warp 1 owns
+// the TMEM accumulator and lane 0 issues tcgen05.mma (M=128, N=BN, K=16, four
+// per stage), committing each stage back to the producer through an mbarrier.
+// With split-K, every CTA writes its fp32 partial tile and the last CTA of a
+// tile (atomic ticket, no spinning) sums the partials in split order, so the
+// result is deterministic and independent of M.  The final tile is staged in
+// shared memory and handed to one of the fused epilogues (bf16/f32 store,
+// residual add + DFlash-2 block conv, SwiGLU, q/k-norm + RoPE + KV routing,
+// per-tile argmax for the LM head).
+//
+// Weight loads are issued before griddepcontrol.wait, so with programmatic
+// dependent launch a GEMM prefetches its first stages of weights while the
+// previous kernel is still draining.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dflash {
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int STAGES = BN <= 16 ? 6 : BN <= 32 ? 5 : BN <= 64 ? 4 : BN <= 128 ? 6 : 4;
+  static constexpr int A_BYTES = kTileN * kTileK * 2;  // 16 KB
+  static constexpr int B_BYTES = BN * kTileK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TS_LD = kTileN + 4;  // staged epilogue tile row stride (floats)
+  static constexpr int TILE_BYTES = BN * TS_LD * 4;
+  static constexpr int PIPE_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int MAIN_BYTES = PIPE_BYTES > TILE_BYTES ? PIPE_BYTES : TILE_BYTES;
+  static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + 1024;
+  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+};
+
+// ---------------------------------------------------------------- RoPE angle
+// sin/cos of pos * inv_freq with inv_freq held as an unevaluated float pair
+// (hi + lo).  The product is formed exactly with an FMA (Dekker's two-product)
+// and reduced modulo 2*pi with a three-piece Cody-Waite split of 2*pi, so the
+// reduced angle is accurate to ~1e-6 rad for positions up to 2^24.
+__device__ __forceinline__ void rope_sincos(int pos, float2 f, float* s, float* c) {
+  const float pf = static_cast<float>(pos);
+  const float a_hi = pf * f.x;
+  const float a_err = fmaf(pf, f.x, -a_hi);
+  const float a_lo = fmaf(pf, f.y, a_err);
+  // 2*pi = P1 + P2 + P3 (P1, P2 with trailing zero bits)
+  constexpr float P1 = 6.28125f;
+  constexpr float P2 = 1.93500518798828125e-3f;
+  constexpr float P3 = 3.019916050561733e-07f;
+  constexpr float INV_2PI = 0.15915494309189535f;
+  const float k = rintf(a_hi * INV_2PI);
+  float r = fmaf(-k, P1, a_hi);
+  r = fmaf(-k, P2, r);
+  r = fmaf(-k, P3, r);
+  r += a_lo;
+  sincosf(r, s, c);
+}
+
+// ---------------------------------------------------------------- epilogues
+template <int BN>
+__device__ void epi_store(const GemmParams& p, const float* ts, int tile, int m0, int rows) {
+  using C = GemmCfg<BN>;
+  const int n0 = tile * kTileN;
+  for (int idx = threadIdx.x; idx < rows * kTileN; idx += 128) {
+    const int r = idx / kTileN, f = idx % kTileN;
+    const float v = ts[r * C::TS_LD + f];
+    const size_t o = static_cast<size_t>(m0 + r) * p.ld_out + n0 + f;
+    if (p.mode == EPI_STORE_BF16)
+      static_cast<uint16_t*>(p.out)[o] = f2bf(v);
+    else
+      static_cast<float*>(p.out)[o] = v;
+  }
+}
+
+template <int BN>
+__device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int rows) {
+  using C = GemmCfg<BN>;
+  const int n0 = tile * kTileN;
+  if (p.conv == nullptr || p.conv_width <= 0) {
+    for (int idx = threadIdx.x; idx < rows * kTileN; idx += 128) {
+      const int r = idx / kTileN, f = idx % kTileN;
+      float* x = p.resid + static_cast<size_t>(m0 + r) * p.ld_resid + n0 + f;
+      *x += ts[r * C::TS_LD + f];
+    }
+    return;
+  }
+  // x_new = x + acc, then x_new += depthwise conv over the block positions
+  // of each request (zero padded), all inside this tile.
+  for (int idx = threadIdx.x; idx < rows * kTileN; idx += 128) {
+    const int r = idx / kTileN, f = idx % kTileN;
+    ts[r * C::TS_LD + f] += p.resid[static_cast<size_t>(m0 + r) * p.ld_resid + n0 + f];
+  }
+  __syncthreads();
+  const int c = (p.conv_width - 1) / 2;
+  for (int idx = threadIdx.x; idx < rows * kTileN; idx += 128) {
+    const int r = idx / kTileN, f = idx % kTileN;
+    const int i = (m0 + r) % p.block;
+    const int rbase = r - i;
+    float y = ts[r * C::TS_LD + f];
+    const uint16_t* w = p.conv + static_cast<size_t>(n0 + f) * p.conv_width;
+    for (int j = 0; j < p.conv_width; ++j) {
+      const int src = i + j - c;
+      if (src >= 0 && src < p.block && rbase + src < rows)
+        y = fmaf(bf2f(w[j]), ts[(rbase + src) * C::TS_LD + f], y);
+    }
+    p.resid[static_cast<size_t>(m0 + r) * p.ld_resid + n0 + f] = y;
+  }
+}
+
+template <int BN>
+__device__ void epi_swiglu(const GemmParams& p, const float* ts, int tile, int m0, int rows) {
+  using C = GemmCfg<BN>;
+  uint16_t* out = static_cast<uint16_t*>(p.out);
+  for (int idx = threadIdx.x; idx < rows * 64; idx += 128) {
+    const int r = idx / 64, j = idx % 64;
+    const float g = ts[r * C::TS_LD + j];
+    const float u = ts[r * C::TS_LD + 64 + j];
+    out[static_cast<size_t>(m0 + r) * p.ld_out + tile * 64 + j] = f2bf(silu_f(g) * u);
+  }
+}
+
+template <int BN>
+__device__ void epi_argmax(const GemmParams& p, const float* ts, int tile, int m0, int rows) {
+  using C = GemmCfg<BN>;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_tiles = gridDim.x;
+  const int n0 = tile * kTileN;
+  for (int r = warp; r < rows; r += 4) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int f = lane + 32 * t;
+      const float v = ts[r * C::TS_LD + f];
+      if (v > bv) { bv = v; bi = n0 + f; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) {
+      p.amax_val[static_cast<size_t>(m0 + r) * n_tiles + tile] = bv;
+      p.amax_idx[static_cast<size_t>(m0 + r) * n_tiles + tile] = bi;
+    }
+  }
+  if (p.logits != nullptr) {
+    for (int idx = threadIdx.x; idx < rows * kTileN; idx += 128) {
+      const int r = idx / kTileN, f = idx % kTileN;
+      p.logits[static_cast<size_t>(m0 + r) * p.ld_logits + n0 + f] = ts[r * C::TS_LD + f];
+    }
+  }
+}
+
+template <int BN>
+__device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, int rows) {
+  using C = GemmCfg<BN>;
+  const QkvEpi& e = p.qkv;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int d = e.head_dim;
+  const int half = d / 2;
+  const int per_tile = kTileN / d;
+  const int npair = half / 32;  // pairs per lane: 1 (d=64) or 2 (d=128)
+  const int hq = e.n_q_heads, hkv = e.n_kv_heads;
+  for (int w = warp; w < rows * per_tile; w += 4) {
+    const int r = w / per_tile, hl = w % per_tile;
+    const int m = m0 + r;
+    const int head = (e.f0 + tile * kTileN + hl * d) / d;
+    const int kind = head < hq ? 0 : (head < hq + hkv ? 1 : 2);
+    const int hidx = kind == 0 ? head : (kind == 1 ? head - hq : head - hq - hkv);
+    const bool is_blk = m < e.n_blk;
+    int req, pos;
+    if (is_blk) {
+      req = m / e.block;
+      pos = e.anchor_pos[req] + m % e.block;
+    } else {
+      const int j = m - e.n_blk;
+      if (e.pool_req != nullptr) {
+        req = e.pool_req[j];
+        pos = e.pool_pos[j];
+      } else {
+        req = j / e.rows_per_req;
+        pos = e.pool_pos0[req] + j % e.rows_per_req;
+      }
+      if (pos < 0) continue;
+      if (kind == 0 && !e.keep_q_pool) continue;
+    }
+    const float* xs = ts + r * C::TS_LD + hl * d;
+    float x1[2], x2[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (t < npair) {
+        x1[t] = xs[lane + 32 * t];
+        x2[t] = xs[lane + 32 * t + half];
+      }
+    }
+    if (kind < 2) {
+      const uint16_t* g = kind == 0 ? e.q_norm : e.k_norm;
+      if (g != nullptr) {
+        float ss = 0.f;
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (t < npair) ss += x1[t] * x1[t] + x2[t] * x2[t];
+        ss = warp_sum(ss);
+        const float inv = rsqrtf(ss / static_cast<float>(d) + e.eps);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t < npair) {
+            x1[t] = x1[t] * inv * bf2f(g[lane + 32 * t]);
+            x2[t] = x2[t] * inv * bf2f(g[lane + 32 * t + half]);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (t < npair) {
+          float sn, cs;
+          rope_sincos(pos, e.rope[lane + 32 * t], &sn, &cs);
+          const float a = x1[t], b = x2[t];
+          x1[t] = a * cs - b * sn;
+          x2[t] = b * cs + a * sn;
+        }
+      }
+    }
+    uint16_t* dst;
+    if (kind == 0) {
+      dst = e.q + (static_cast<size_t>(m) * hq + hidx) * d;
+    } else if (is_blk) {
+      dst = (kind == 1 ? e.kblk : e.vblk) +
+            ((static_cast<size_t>(req) * hkv + hidx) * e.block + m % e.block) * d;
+    } else {
+      const int pi = pos / e.page_size;
+      const int pg = pi < e.max_pages ? e.page_table[static_cast<size_t>(req) * e.max_pages + pi] : -1;
+      if (pg < 0 || pg >= e.n_pages) {
+        if (lane == 0) raise_status(p.status, DFLASH_ERR_CAPACITY, 101);
+        continue;
+      }
+      dst = e.pool + ((((static_cast<size_t>(pg) * 2 + (kind - 1)) * hkv + hidx) * e.page_size) +
+                      pos % e.page_size) * d;
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (t < npair) {
+        dst[lane + 32 * t] = f2bf(x1[t]);
+        dst[lane + 32 * t + half] = f2bf(x2[t]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+template <int BN>
+__global__ void __launch_bounds__(128, 1)
+    gemm_tc05_kernel(const __grid_constant__ CUtensorMap wmap,
+                     const __grid_constant__ CUtensorMap xmap, const __grid_constant__ GemmParams p) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::MAIN_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* done = empty + C::STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  float* ts = reinterpret_cast<float*>(smem);  // staged tile (after the mainloop)
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int tile = blockIdx.x, split = blockIdx.y, mt = blockIdx.z;
+  const int m0 = mt * BN;
+  const int kb0 = split * p.kb_per_split;
+  const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+  const int nkb = kb1 - kb0;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&wmap);
+    tma_prefetch_desc(&xmap);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  griddep_launch_dependents();
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_x = l2_policy_evict_last();
+    const int wrow = p.w_row0 + tile * p.w_tile_step;
+    const int pre = nkb < C::STAGES ? nkb : C::STAGES;
+    for (int it = 0; it < pre; ++it) {
+      uint8_t* a = smem + it * C::A_BYTES;
+      const int kx = (kb0 + it) * kTileK;
+      mbar_arrive_expect_tx(&full[it], C::STAGE_BYTES);
+      tma_load_2d(a, &wmap, kx, wrow, &full[it], pol_w);
+      tma_load_2d(a + C::A_BYTES / 2, &wmap, kx, wrow + p.w_half_gap, &full[it], pol_w);
+    }
+    griddep_wait();  // activations come from the previous kernel
+    for (int it = 0; it < pre; ++it) {
+      uint8_t* b = smem + C::STAGES * C::A_BYTES + it * C::B_BYTES;
+      tma_load_2d(b, &xmap, (kb0 + it) * kTileK, m0, &full[it], pol_x);
+    }
+    for (int it = pre; it < nkb; ++it) {
+      const int s = it % C::STAGES;
+      const uint32_t ph = ((it / C::STAGES) & 1) ^ 1;
+      if (!mbar_wait(&empty[s], ph, abort_flag)) {
+        *abort_flag = 1;
+        raise_status(p.status, DFLASH_ERR_TIMEOUT, 11);
+        break;
+      }
+      uint8_t* a = smem + s * C::A_BYTES;
+      uint8_t* b = smem + C::STAGES * C::A_BYTES + s * C::B_BYTES;
+      const int kx = (kb0 + it) * kTileK;
+      mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+      tma_load_2d(a, &wmap, kx, wrow, &full[s], pol_w);
+      tma_load_2d(a + C::A_BYTES / 2, &wmap, kx, wrow + p.w_half_gap, &full[s], pol_w);
+      tma_load_2d(b, &xmap, kx, m0, &full[s], pol_x);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer (single thread)
+    constexpr uint32_t idesc = umma_idesc_bf16(kTileN, BN);
+    for (int it = 0; it < nkb; ++it) {
+      const int s = it % C::STAGES;
+      const uint32_t ph = (it / C::STAGES) & 1;
+      if (!mbar_wait(&full[s], ph, abort_flag)) {
+        *abort_flag = 1;
+        raise_status(p.status, DFLASH_ERR_TIMEOUT, 12);
+        break;
+      }
+      tc_fence_after();
+      const uint64_t ad = umma_desc_sw128(smem_u32(smem + s * C::A_BYTES));
+      const uint64_t bd = umma_desc_sw128(smem_u32(smem + C::STAGES * C::A_BYTES + s * C::B_BYTES));
+#pragma unroll
+      for (int k = 0; k < kTileK / 16; ++k)
+        umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (it | k) != 0 ? 1u : 0u);
+      umma_commit(&empty[s]);
+    }
+    umma_commit(done);
+  }
+  if (!(warp == 0 && lane == 0)) griddep_wait();
+  __syncwarp();
+
+  // ---------------- epilogue: TMEM -> (partials | staged tile)
+  const bool ok = mbar_wait(done, 0, abort_flag);
+  if (!ok) {
+    *abort_flag = 1;
+    if (lane == 0) raise_status(p.status, DFLASH_ERR_TIMEOUT, 13);
+  }
+  __syncthreads();
+  const bool aborted = *abort_flag != 0;
+  tc_fence_after();
+  const int rows = min(BN, p.M - m0);
+  const int f = warp * 32 + lane;
+  const int n0 = tile * kTileN;
+  bool do_epi = false;
+  if (!aborted) {
+    if (p.splits > 1) {
+      float* part = p.partial + static_cast<size_t>(split) * p.M * p.N;
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 16, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = c * 16 + j;
+          if (r < rows) part[static_cast<size_t>(m0 + r) * p.N + n0 + f] = v[j];
+        }
+      }
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        const int prev = atomicAdd(&p.counters[mt * gridDim.x + tile], 1);
+        *last_flag = (prev == p.splits - 1) ? 1 : 0;
+      }
+      __syncthreads();
+      if (*last_flag) {
+        __threadfence();
+        for (int r = 0; r < rows; ++r) {
+          float s = 0.f;
+          for (int sp = 0; sp < p.splits; ++sp)
+            s += __ldcg(p.partial + (static_cast<size_t>(sp) * p.M + m0 + r) * p.N + n0 + tid);
+          ts[r * C::TS_LD + tid] = s;
+        }
+        if (tid == 0) p.counters[mt * gridDim.x + tile] = 0;
+        do_epi = true;
+      }
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 16, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ts[(c * 16 + j) * C::TS_LD + f] = v[j];
+      }
+      do_epi = true;
+    }
+  }
+  __syncthreads();
+  if (do_epi) {
+    switch (p.mode) {
+      case EPI_STORE_BF16:
+      case EPI_STORE_F32: epi_store<BN>(p, ts, tile, m0, rows); break;
+      case EPI_RESID: epi_resid<BN>(p, ts, tile, m0, rows); break;
+      case EPI_SWIGLU: epi_swiglu<BN>(p, ts, tile, m0, rows); break;
+      case EPI_ARGMAX: epi_argmax<BN>(p, ts, tile, m0, rows); break;
+      case EPI_QKV: epi_qkv<BN>(p, ts, tile, m0, rows); break;
+      default: break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+int gemm_bn_for(int M) {
+  return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+}
+
+int gemm_max_smem_bytes() {
+  int m = GemmCfg<16>::SMEM_BYTES;
+  m = m > GemmCfg<32>::SMEM_BYTES ? m : GemmCfg<32>::SMEM_BYTES;
+  m = m > GemmCfg<64>::SMEM_BYTES ? m : GemmCfg<64>::SMEM_BYTES;
+  m = m > GemmCfg<128>::SMEM_BYTES ? m : GemmCfg<128>::SMEM_BYTES;
+  m = m > GemmCfg<256>::SMEM_BYTES ? m : GemmCfg<256>::SMEM_BYTES;
+  return m;
+}
+
+template <int BN>
+static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
+                             const GemmParams& p, cudaStream_t s, bool pdl) {
+  using C = GemmCfg<BN>;
+  static thread_local int attr_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc05_kernel<BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_device = dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.N / kTileN, p.splits, (p.M + BN - 1) / BN);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_tc05_kernel<BN>, *w_map, *x_map, p);
+}
+
+cudaError_t gemm_launch(const CUtensorMap* w_map, const CUtensorMap* x_map, const GemmParams& p,
+                        int bn, cudaStream_t s, bool pdl) {
+  switch (bn) {
+    case 16: return launch_bn<16>(w_map, x_map, p, s, pdl);
+    case 32: return launch_bn<32>(w_map, x_map, p, s, pdl);
+    case 64: return launch_bn<64>(w_map, x_map, p, s, pdl);
+    case 128: return launch_bn<128>(w_map, x_map, p, s, pdl);
+    case 256: return launch_bn<256>(w_map, x_map, p, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dflash

@@ -1,0 +1,122 @@
+// Internal launch interface between the C ABI (dflash_api.cu) and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dflash {
+
+constexpr int kTileN = 128;      // weight rows per CTA tile (MMA M)
+constexpr int kTileK = 64;       // K elements per pipeline stage (one 128-B swizzle row)
+constexpr int kMaxRopePairs = 64;
+
+enum EpiMode : int {
+  EPI_STORE_BF16 = 0,  // out[m][n] = bf16(acc)
+  EPI_STORE_F32 = 1,   // out[m][n] = acc
+  EPI_RESID = 2,       // resid[m][n] += acc, then optional block conv
+  EPI_SWIGLU = 3,      // out[m][j] = bf16(silu(gate) * up)
+  EPI_QKV = 4,         // q/k norm + RoPE, route to q / block K,V / paged pool
+  EPI_ARGMAX = 5,      // per-tile (max, argmax) per row (+ optional f32 logits)
+};
+
+struct QkvEpi {
+  int n_blk;             // rows [0, n_blk) are block rows: request m / block, position anchor_pos + m % block
+  int block;
+  const int32_t* anchor_pos;
+  int rows_per_req;      // pool rows (m >= n_blk): request (m - n_blk) / rows_per_req ... when pool_req == null
+  const int32_t* pool_pos0;   // [batch] first position of each request's pool rows (target rows)
+  const int32_t* pool_req;    // [rows] explicit request of each pool row (context rows), or null
+  const int32_t* pool_pos;    // [rows] explicit position (< 0 = skip), or null
+  int keep_q_pool;       // pool rows also store q (target forward)
+  int n_q_heads, n_kv_heads, head_dim;
+  int f0;                // feature index (in q|k|v space) of this launch's output feature 0
+  const uint16_t* q_norm;  // [d] or null
+  const uint16_t* k_norm;  // [d] or null
+  float eps;
+  uint16_t* q;           // [rows][hq][d]
+  uint16_t* kblk;        // [batch][hkv][block][d]
+  uint16_t* vblk;
+  uint16_t* pool;        // layer base [n_pages][2][hkv][page][d]
+  const int32_t* page_table;
+  int max_pages, n_pages, page_size;
+  float2 rope[kMaxRopePairs];  // inv_freq of pair p as (hi, lo) float pair
+};
+
+struct GemmParams {
+  int M, N, K;           // activation rows, output features (this launch), reduction
+  int w_row0;            // tensor-map row of output tile 0, half 0
+  int w_tile_step;       // tensor-map rows advanced per output tile
+  int w_half_gap;        // tensor-map row distance between the two 64-row halves
+  int kb_total, kb_per_split, splits;
+  float* partial;        // [splits][M][N] (splits > 1)
+  int32_t* counters;     // [n_tiles * m_tiles], zero between launches
+  int32_t* status;
+  int mode;
+  void* out;             // bf16/f32 store or SwiGLU output
+  int ld_out;
+  float* resid;
+  int ld_resid;
+  const uint16_t* conv;  // [N][conv_width] (this layer) or null
+  int conv_width, block;
+  float* logits;         // argmax mode: optional [M][ld_logits]
+  int ld_logits;
+  float* amax_val;       // [M][n_tiles]
+  int32_t* amax_idx;
+  QkvEpi qkv;
+};
+
+// Picks the MMA N width for M rows and the split-K count.
+int gemm_bn_for(int M);
+int gemm_max_smem_bytes();
+cudaError_t gemm_launch(const CUtensorMap* w_map, const CUtensorMap* x_map, const GemmParams& p,
+                        int bn, cudaStream_t s, bool pdl);
+
+struct AttnParams {
+  const uint16_t* q;     // [batch*n][hq][d]
+  int batch, n;          // requests, query rows per request
+  const int32_t* pos0;   // [batch] position of each request's row 0
+  int causal;            // 1: row at pos attends keys [0, pos] of the pool; 0: [0, pos0) + block keys
+  const uint16_t* pool;  // layer base
+  const int32_t* page_table;
+  int max_pages, n_pages, page_size;
+  const uint16_t* kblk;  // [batch][hkv][n][d] (non-causal)
+  const uint16_t* vblk;
+  int hq, hkv, d;
+  int split_keys;        // keys per split, multiple of 64
+  int n_splits;          // grid.x
+  float* o_part;         // [n_splits][batch*n][hq][d]
+  float* ml_part;        // [n_splits][batch*n][hq][2]
+  uint16_t* out;         // [batch*n][hq][d]
+  int32_t* status;
+};
+cudaError_t attention_launch(const AttnParams& p, cudaStream_t s, bool pdl);
+size_t attention_part_floats(int n_splits, int rows, int hq, int d);
+
+// small kernels (small_kernels.cu)
+cudaError_t embed_block_launch(const int32_t* anchor, int batch, int block, const uint16_t* embed,
+                               const uint16_t* mask_embed, const uint16_t* norm, float eps,
+                               int hidden, float* x, uint16_t* a, int ld_a,
+                               const uint16_t* pending, int T, cudaStream_t s, bool pdl,
+                               int32_t* status, int vocab);
+cudaError_t embed_tokens_launch(const int32_t* tokens, int rows, const uint16_t* embed,
+                                const uint16_t* norm, float eps, int hidden, float* x,
+                                uint16_t* a, cudaStream_t s, bool pdl, int32_t* status,
+                                int vocab);
+cudaError_t rmsnorm_launch(const float* x, int rows, int hidden, const uint16_t* g, float eps,
+                           uint16_t* out, int ld_out, uint16_t* raw_out, int ld_raw,
+                           cudaStream_t s, bool pdl);
+cudaError_t argmax_reduce_launch(const float* val, const int32_t* idx, int rows, int n_tiles,
+                                 int block, int32_t* out, int skip_first, cudaStream_t s,
+                                 bool pdl);
+cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int batch, int B,
+                          int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
+                          int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
+                          const int32_t* anchor_pos_in, int32_t* anchor_pos_out, cudaStream_t s,
+                          bool pdl);
+cudaError_t synth_target_launch(const int32_t* draft, int batch, int B, const uint64_t* thr,
+                                int vocab, uint64_t seed, int64_t* step, int advance,
+                                int32_t* target, cudaStream_t s, bool pdl);
+cudaError_t copy_rows_f32_launch(const float* src, float* dst, size_t n, cudaStream_t s, bool pdl);
+
+}  // namespace dflash

@@ -1,0 +1,299 @@
+// Row-wise and integer kernels of the draft step: block embedding, RMSNorm,
+// LM-head argmax reduction, greedy verify and the synthetic target stand-in.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dflash {
+
+static cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          bool pdl, Args... args) {
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (threadIdx.x < 32) {
+    t = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0.f;
+    t = warp_sum(t);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  t = red[0];
+  __syncthreads();
+  return t;
+}
+
+// x[r] = E[anchor] (block position 0) or mask_embed (positions 1..B-1);
+// a[r] = bf16(RMSNorm(x[r]) * g).  Blocks past the block rows copy the
+// pending context rows into a[n_blk + t] so the first QKV GEMM sees
+// [block rows ; context rows] as one operand.
+__global__ void __launch_bounds__(kRowThreads)
+    embed_block_kernel(const int32_t* anchor, int block, int n_blk, const uint16_t* embed,
+                       const uint16_t* mask_embed, const uint16_t* g, float eps, int H, float* x,
+                       uint16_t* a, int ld_a, const uint16_t* pending, int32_t* status, int vocab) {
+  __shared__ float red[32];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int r = blockIdx.x;
+  if (r >= n_blk) {
+    const uint16_t* src = pending + static_cast<size_t>(r - n_blk) * H;
+    uint16_t* dst = a + static_cast<size_t>(r) * ld_a;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) dst[i] = src[i];
+    return;
+  }
+  const int req = r / block, i = r % block;
+  const uint16_t* src = mask_embed;
+  if (i == 0) {
+    int tok = anchor[req];
+    if (tok < 0 || tok >= vocab) {
+      if (threadIdx.x == 0) raise_status(status, DFLASH_ERR_INVALID_ARG, 301);
+      tok = 0;
+    }
+    src = embed + static_cast<size_t>(tok) * H;
+  }
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) {
+    const float v = bf2f(src[c]);
+    x[static_cast<size_t>(r) * H + c] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
+  for (int c = threadIdx.x; c < H; c += blockDim.x)
+    a[static_cast<size_t>(r) * ld_a + c] = f2bf(bf2f(src[c]) * inv * bf2f(g[c]));
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+    embed_tokens_kernel(const int32_t* tokens, const uint16_t* embed, const uint16_t* g, float eps,
+                        int H, float* x, uint16_t* a, int32_t* status, int vocab) {
+  __shared__ float red[32];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int r = blockIdx.x;
+  int tok = tokens[r];
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) raise_status(status, DFLASH_ERR_INVALID_ARG, 302);
+    tok = 0;
+  }
+  const uint16_t* src = embed + static_cast<size_t>(tok) * H;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) {
+    const float v = bf2f(src[c]);
+    x[static_cast<size_t>(r) * H + c] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
+  for (int c = threadIdx.x; c < H; c += blockDim.x)
+    a[static_cast<size_t>(r) * H + c] = f2bf(bf2f(src[c]) * inv * bf2f(g[c]));
+}
+
+// out[r] = bf16(x[r] * g / sqrt(mean(x[r]^2) + eps)); raw_out[r] = bf16(x[r]).
+__global__ void __launch_bounds__(kRowThreads)
+    rmsnorm_kernel(const float* x, int H, const uint16_t* g, float eps, uint16_t* out, int ld_out,
+                   uint16_t* raw_out, int ld_raw) {
+  __shared__ float red[32];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int r = blockIdx.x;
+  const float* xr = x + static_cast<size_t>(r) * H;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) {
+    const float v = xr[c];
+    ss += v * v;
+    if (raw_out != nullptr) raw_out[static_cast<size_t>(r) * ld_raw + c] = f2bf(v);
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
+  for (int c = threadIdx.x; c < H; c += blockDim.x)
+    out[static_cast<size_t>(r) * ld_out + c] = f2bf(xr[c] * inv * bf2f(g[c]));
+}
+
+// One warp per row: (max, lowest index) over the per-tile partials.
+__global__ void __launch_bounds__(128)
+    argmax_reduce_kernel(const float* val, const int32_t* idx, int rows, int n_tiles, int block,
+                         int32_t* out, int skip_first) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int row = blockIdx.x * 4 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  const int i = row % block;
+  if (skip_first && i == 0) return;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int t = lane; t < n_tiles; t += 32) {
+    const float v = val[static_cast<size_t>(row) * n_tiles + t];
+    const int j = idx[static_cast<size_t>(row) * n_tiles + t];
+    if (v > bv || (v == bv && j < bi)) { bv = v; bi = j; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+  }
+  if (lane == 0) {
+    if (skip_first)
+      out[(row / block) * (block - 1) + i - 1] = bi;
+    else
+      out[row] = bi;
+  }
+}
+
+// One warp per request: ballot of mismatches, n = index of the first one.
+__global__ void __launch_bounds__(128)
+    verify_kernel(const int32_t* draft, const int32_t* target, int batch, int B,
+                  int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
+                  int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
+                  const int32_t* anchor_pos_in, int32_t* anchor_pos_out) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int r = blockIdx.x * 4 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (r >= batch) return;
+  const int t = lane < B ? target[static_cast<size_t>(r) * B + lane] : 0;
+  const bool mism = lane < B - 1 && draft[static_cast<size_t>(r) * (B - 1) + lane] != t;
+  const unsigned mask = __ballot_sync(0xffffffffu, mism);
+  const int n = mask ? __ffs(mask) - 1 : B - 1;
+  const int bonus = __shfl_sync(0xffffffffu, t, n);
+  const int tl = (lane == 0 && tgt_len_in != nullptr) ? tgt_len_in[r] : 0;
+  const int ap = (lane == 0 && anchor_pos_in != nullptr) ? anchor_pos_in[r] : 0;
+  __syncwarp();
+  if (lane < B && out_tokens != nullptr)
+    out_tokens[static_cast<size_t>(r) * B + lane] = lane <= n ? t : -1;
+  if (lane == 0) {
+    if (n_accept != nullptr) n_accept[r] = n;
+    if (tgt_len_out != nullptr) tgt_len_out[r] = tl + n + 1;
+    if (ctx_pending != nullptr) ctx_pending[r] = n + 1;
+    if (anchor_out != nullptr) anchor_out[r] = bonus;
+    if (anchor_pos_out != nullptr) anchor_pos_out[r] = ap + n + 1;
+  }
+}
+
+// ---- synthetic target (counter-based, splitmix64 output function)
+__device__ __forceinline__ uint64_t splitmix64(uint64_t z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+__device__ __forceinline__ uint64_t synth_key(uint64_t seed, uint64_t step, uint64_t r, uint64_t i,
+                                              uint64_t stream) {
+  constexpr uint64_t M = 0x100000001B3ull;
+  uint64_t k = seed;
+  k = k * M + step;
+  k = k * M + r;
+  k = k * M + i;
+  k = k * M + stream;
+  return k;
+}
+
+__global__ void synth_target_kernel(const int32_t* draft, int batch, int B, const uint64_t* thr,
+                                    int vocab, uint64_t seed, int64_t* step, int advance,
+                                    int32_t* target) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const uint64_t st = static_cast<uint64_t>(*step);
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < batch * B; idx += blockDim.x) {
+    const int r = idx / B, i = idx % B;
+    const uint64_t h0 = splitmix64(synth_key(seed, st, r, i, 0));
+    const uint64_t h1 = splitmix64(synth_key(seed, st, r, i, 1));
+    int32_t t;
+    if (i < B - 1) {
+      const int32_t d = draft[static_cast<size_t>(r) * (B - 1) + i];
+      if ((h0 >> 11) < thr[r])
+        t = d;
+      else
+        t = static_cast<int32_t>((static_cast<uint64_t>(d) + 1 + h1 % static_cast<uint64_t>(vocab - 1)) %
+                                 static_cast<uint64_t>(vocab));
+    } else {
+      t = static_cast<int32_t>(h1 % static_cast<uint64_t>(vocab));
+    }
+    target[idx] = t;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && advance) *step = static_cast<int64_t>(st + 1);
+}
+
+__global__ void copy_f32_kernel(const float* src, float* dst, size_t n) {
+  griddep_launch_dependents();
+  griddep_wait();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    dst[i] = src[i];
+}
+
+// ---------------------------------------------------------------- launchers
+cudaError_t embed_block_launch(const int32_t* anchor, int batch, int block, const uint16_t* embed,
+                               const uint16_t* mask_embed, const uint16_t* norm, float eps,
+                               int hidden, float* x, uint16_t* a, int ld_a,
+                               const uint16_t* pending, int T, cudaStream_t s, bool pdl,
+                               int32_t* status, int vocab) {
+  const int nb = batch * block;
+  return launch(embed_block_kernel, dim3(nb + T), dim3(kRowThreads), 0, s, pdl, anchor, block, nb,
+                embed, mask_embed, norm, eps, hidden, x, a, ld_a, pending, status, vocab);
+}
+cudaError_t embed_tokens_launch(const int32_t* tokens, int rows, const uint16_t* embed,
+                                const uint16_t* norm, float eps, int hidden, float* x,
+                                uint16_t* a, cudaStream_t s, bool pdl, int32_t* status,
+                                int vocab) {
+  return launch(embed_tokens_kernel, dim3(rows), dim3(kRowThreads), 0, s, pdl, tokens, embed, norm,
+                eps, hidden, x, a, status, vocab);
+}
+cudaError_t rmsnorm_launch(const float* x, int rows, int hidden, const uint16_t* g, float eps,
+                           uint16_t* out, int ld_out, uint16_t* raw_out, int ld_raw,
+                           cudaStream_t s, bool pdl) {
+  return launch(rmsnorm_kernel, dim3(rows), dim3(kRowThreads), 0, s, pdl, x, hidden, g, eps, out,
+                ld_out, raw_out, ld_raw);
+}
+cudaError_t argmax_reduce_launch(const float* val, const int32_t* idx, int rows, int n_tiles,
+                                 int block, int32_t* out, int skip_first, cudaStream_t s,
+                                 bool pdl) {
+  return launch(argmax_reduce_kernel, dim3((rows + 3) / 4), dim3(128), 0, s, pdl, val, idx, rows,
+                n_tiles, block, out, skip_first);
+}
+cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int batch, int B,
+                          int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
+                          int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
+                          const int32_t* anchor_pos_in, int32_t* anchor_pos_out, cudaStream_t s,
+                          bool pdl) {
+  return launch(verify_kernel, dim3((batch + 3) / 4), dim3(128), 0, s, pdl, draft, target, batch,
+                B, out_tokens, n_accept, tgt_len_in, tgt_len_out, ctx_pending, anchor_out,
+                anchor_pos_in, anchor_pos_out);
+}
+cudaError_t synth_target_launch(const int32_t* draft, int batch, int B, const uint64_t* thr,
+                                int vocab, uint64_t seed, int64_t* step, int advance,
+                                int32_t* target, cudaStream_t s, bool pdl) {
+  return launch(synth_target_kernel, dim3(1), dim3(1024), 0, s, pdl, draft, batch, B, thr, vocab,
+                seed, step, advance, target);
+}
+cudaError_t copy_rows_f32_launch(const float* src, float* dst, size_t n, cudaStream_t s, bool pdl) {
+  const int blocks = static_cast<int>((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+  return launch(copy_f32_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, s, pdl, src, dst, n);
+}
+
+}  // namespace dflash

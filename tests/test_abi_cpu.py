@@ -1,0 +1,106 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports
+every symbol the header declares, and rejects bad arguments before launching
+anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_diffusion_speculative_fuse_gb300 import _build, binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return B.load()
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "dflash.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dflash_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary_calls():
+    syms = header_symbols()
+    for s in ("dflash_ctx_fuse", "dflash_kv_append", "dflash_draft_block",
+              "dflash_verify_greedy"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for s in header_symbols():
+        assert hasattr(lib, s), s
+        assert s in B.EXPORTS, f"binding misses {s}"
+
+
+def test_strerror_codes(lib):
+    assert B.strerror(0) == "ok"
+    assert "invalid" in B.strerror(-1)
+    assert "capacity" in B.strerror(-3)
+    assert B.strerror(-99) == "unknown error"
+
+
+def test_model_create_rejects_bad_args(lib):
+    h = ctypes.c_void_p()
+    assert lib.dflash_model_create(None, None, ctypes.byref(h)) == -1
+    cfg = B.DflashConfig(n_layers=1, hidden=100, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                         mlp=256, vocab=1024, block=8, n_taps=2, conv_width=0, qk_norm=1,
+                         fc_norm=1, page_size=16, rms_eps=1e-6, rope_base=1e4)
+    w = B.DflashWeights()
+    assert lib.dflash_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -2
+    cfg.hidden = 256
+    cfg.head_dim = 96
+    assert lib.dflash_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -2
+    cfg.head_dim = 64
+    cfg.block = 33
+    assert lib.dflash_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -2
+    cfg.block = 8
+    cfg.conv_width = 2
+    assert lib.dflash_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -2
+    cfg.conv_width = 0
+    # valid shape, missing weight pointers
+    assert lib.dflash_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -1
+    w.embed = 0x1001  # misaligned
+    assert lib.dflash_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -1
+
+
+def test_verify_rejects_bad_sizes(lib):
+    f = lib.dflash_verify_greedy
+    dummy = ctypes.c_void_p(0x1000)
+    assert f(dummy, dummy, 0, 16, *([None] * 8), None) == -1      # batch 0
+    assert f(dummy, dummy, 1, 0, *([None] * 8), None) == -1       # B 0
+    assert f(dummy, dummy, 1, 33, *([None] * 8), None) == -1      # B > 32
+    assert f(None, dummy, 1, 4, *([None] * 8), None) == -1        # drafts missing
+    # an output length without its input
+    args = [None] * 8
+    args[3] = dummy
+    assert f(dummy, dummy, 1, 4, *args, None) == -1
+
+
+def test_synth_target_rejects_bad_sizes(lib):
+    f = lib.dflash_synth_target
+    d = ctypes.c_void_p(0x1000)
+    assert f(d, 64, 32, d, 100, 1, d, 1, d, None) == -1          # batch*B > 1024
+    assert f(d, 1, 4, d, 1, 1, d, 1, d, None) == -1               # vocab < 2
+    assert f(d, 1, 4, None, 100, 1, d, 1, d, None) == -1          # no thresholds
+
+
+def test_workspace_init_rejects_misaligned(lib):
+    assert lib.dflash_workspace_init(ctypes.c_void_p(0x1004), 1 << 20, None) == -1
+    assert lib.dflash_workspace_init(ctypes.c_void_p(0x1000), 16, None) == -1
+
+
+def test_compute_calls_reject_null_handle(lib):
+    d = ctypes.c_void_p(0x1000)
+    assert lib.dflash_ctx_fuse(None, d, 4, d, d, 1 << 20, None) == -1
+    kv = B.DflashKV()
+    assert lib.dflash_kv_append(None, d, d, d, 4, ctypes.byref(kv), d, 1 << 20, None) == -1
+    assert lib.dflash_draft_block(None, d, d, 1, ctypes.byref(kv), None, None, None, 0, d,
+                                  None, None, d, 1 << 20, None) == -1
+    assert lib.dflash_target_forward(None, d, d, 1, 1, ctypes.byref(kv), None, 0, None, d,
+                                     None, d, 1 << 20, None) == -1
+    assert lib.dflash_workspace_bytes(None, 16, 16, 1, 128) == 0
