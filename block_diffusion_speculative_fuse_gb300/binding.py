@@ -86,6 +86,10 @@ EXPORTS = {
                                              ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                              ctypes.c_void_p]),
+    "dflash_kernel_launches": (ctypes.c_uint64, []),
+    "dflash_lm_head_argmax": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_size_t, ctypes.c_void_p]),
     "dflash_synth_target": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64,
                                            ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
@@ -219,3 +223,13 @@ def dflash_synth_target(draft, batch, B, threshold, vocab, seed, step, advance, 
     return _check("dflash_synth_target", load().dflash_synth_target(
         ptr(draft), batch, B, ptr(threshold), vocab, ctypes.c_uint64(seed), ptr(step),
         int(advance), ptr(target), stream_handle(stream)))
+
+
+def dflash_lm_head_argmax(h, x, rows, argmax, logits, ws, stream=None):
+    return _check("dflash_lm_head_argmax", load().dflash_lm_head_argmax(
+        h, ptr(x), rows, ptr(argmax), ptr(logits), ptr(ws), ws.numel() * ws.element_size(),
+        stream_handle(stream)))
+
+
+def dflash_kernel_launches() -> int:
+    return int(load().dflash_kernel_launches())

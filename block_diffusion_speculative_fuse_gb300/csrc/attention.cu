@@ -350,6 +350,7 @@ static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  count_launch();
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_kernel<D, NW>, p);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t c2 = {};
@@ -359,6 +360,7 @@ static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
   c2.stream = s;
   c2.attrs = attr;
   c2.numAttrs = pdl ? 1 : 0;
+  count_launch();
   return cudaLaunchKernelEx(&c2, attn_combine_kernel<D>, p);
 }
 

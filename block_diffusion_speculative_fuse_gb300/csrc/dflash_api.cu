@@ -444,6 +444,8 @@ const char* dflash_strerror(int code) {
 
 int dflash_last_cuda_error(void) { return g_last_cuda; }
 
+uint64_t dflash_kernel_launches(void) { return dflash::launch_count(); }
+
 int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflash_model* out) {
   if (cfg == nullptr || w == nullptr || out == nullptr) return DFLASH_ERR_INVALID_ARG;
   *out = nullptr;
@@ -660,6 +662,24 @@ int dflash_draft_block(dflash_model m, const int32_t* anchor, const int32_t* anc
   if (hidden != nullptr)
     DF_CUDA(copy_rows_f32_launch(b.x, hidden, static_cast<size_t>(rows) * c.hidden, s, true));
   return DFLASH_OK;
+}
+
+int dflash_lm_head_argmax(dflash_model m, const void* x, int32_t rows, int32_t* argmax,
+                          float* logits, void* ws, size_t ws_bytes, void* stream) {
+  if (m == nullptr || x == nullptr || rows < 1 || argmax == nullptr || ws == nullptr ||
+      (reinterpret_cast<uintptr_t>(ws) & 255) || !aligned16(x))
+    return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = m->cfg;
+  Ws w;
+  w.base = static_cast<uint8_t*>(ws);
+  StackBufs b;
+  std::memset(&b, 0, sizeof(b));
+  const int vt = c.vocab / kTileN;
+  b.amax_val = w.take<float>(static_cast<size_t>(rows) * vt);
+  b.amax_idx = w.take<int32_t>(static_cast<size_t>(rows) * vt);
+  if (w.off > ws_bytes) return DFLASH_ERR_CAPACITY;
+  b.a2 = static_cast<uint16_t*>(const_cast<void*>(x));
+  return run_lm_head(m, w, b, rows, 1, 0, argmax, logits, static_cast<cudaStream_t>(stream));
 }
 
 int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t batch, int32_t B,

@@ -11,6 +11,10 @@ constexpr int kTileN = 128;      // weight rows per CTA tile (MMA M)
 constexpr int kTileK = 64;       // K elements per pipeline stage (one 128-B swizzle row)
 constexpr int kMaxRopePairs = 64;
 
+// Host-side count of kernel launches issued by this library.
+uint64_t launch_count();
+void count_launch();
+
 enum EpiMode : int {
   EPI_STORE_BF16 = 0,  // out[m][n] = bf16(acc)
   EPI_STORE_F32 = 1,   // out[m][n] = acc

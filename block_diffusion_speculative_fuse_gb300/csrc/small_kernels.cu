@@ -1,9 +1,15 @@
 // Row-wise and integer kernels of the draft step: block embedding, RMSNorm,
 // LM-head argmax reduction, greedy verify and the synthetic target stand-in.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace dflash {
+
+static std::atomic<uint64_t> g_launches{0};
+uint64_t launch_count() { return g_launches.load(); }
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 static cudaLaunchAttribute pdl_attr() {
   cudaLaunchAttribute a;
@@ -23,6 +29,7 @@ static cudaError_t launch(void (*k)(KArgs...), dim3 grid, dim3 block, size_t sme
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
 }
 

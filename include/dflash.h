@@ -147,6 +147,9 @@ int dflash_workspace_init(void* ws, size_t ws_bytes, void* stream);
  * raising kernel's site id (may be NULL). */
 int dflash_get_status(const void* ws, int32_t* status, int32_t* site, void* stream);
 const char* dflash_strerror(int code);
+/* Number of kernels this library has launched from the host in this process
+ * (launches replayed from a captured CUDA graph are not counted). */
+uint64_t dflash_kernel_launches(void);
 /* CUDA error code of the last DFLASH_ERR_CUDA on this thread (0 if none). */
 int dflash_last_cuda_error(void);
 
@@ -181,6 +184,13 @@ int dflash_draft_block(dflash_model m, const int32_t* anchor, const int32_t* anc
                        const int32_t* pending_req, const int32_t* pending_pos, int32_t T,
                        int32_t* draft, float* logits, float* hidden, void* ws,
                        size_t ws_bytes, void* stream);
+
+/* Shared LM head + argmax alone: argmax[r] = argmax_v (x[r] . lm_head[v]) for
+ * `rows` rows of already final-normed hidden states x (bf16 [rows][hidden]);
+ * lowest index on ties; optional fp32 logits [rows][vocab].  The same
+ * kernels dflash_draft_block runs for its last step. */
+int dflash_lm_head_argmax(dflash_model m, const void* x, int32_t rows, int32_t* argmax,
+                          float* logits, void* ws, size_t ws_bytes, void* stream);
 
 /* Greedy verify of `batch` requests, block size B (1..32).
  * draft int32 [batch][B-1]; target int32 [batch][B] (target[r][j-1] = the
