@@ -133,6 +133,8 @@ struct StackBufs {
   float* amax_val;
   int32_t* amax_idx;
   float* ctx_f32;
+  float* ssq_a;    // [rows][H/128] per-tile sums of squares of the rows behind `a`
+  float* ssq_a2;   // same for `a2`
 };
 
 struct GemmShape {
@@ -192,6 +194,8 @@ void layout_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int 
   b.amax_val = ws.take<float>(static_cast<size_t>(rows) * vt);
   b.amax_idx = ws.take<int32_t>(static_cast<size_t>(rows) * vt);
   b.ctx_f32 = nullptr;
+  b.ssq_a = ws.take<float>(static_cast<size_t>(rows) * (c.hidden / kTileN));
+  b.ssq_a2 = ws.take<float>(static_cast<size_t>(rows) * (c.hidden / kTileN));
 }
 
 GemmParams gemm_base(const dflash_model_s* m, int M, int N, int K, int bn, Ws& ws) {
@@ -265,8 +269,31 @@ int check_kv(const dflash_model_s* m, const dflash_kv* kv) {
   return DFLASH_OK;
 }
 
-// One decoder-layer stack pass (embedding already done: b.x / b.a filled).
-// draft: block rows (non-causal, block K/V), else target rows (causal).
+void set_norm_in(const dflash_model_s* m, GemmParams& p, const float* ssq, int norm_rows) {
+  p.ssq_in = ssq;
+  p.ssq_in_tiles = m->cfg.hidden / kTileN;
+  p.norm_rows = norm_rows;
+  p.norm_dim = m->cfg.hidden;
+  p.norm_eps = m->cfg.rms_eps;
+}
+
+void set_resid_out(const dflash_model_s* m, GemmParams& p, float* x, const uint16_t* gnext,
+                   uint16_t* xg, float* ssq) {
+  p.mode = EPI_RESID;
+  p.resid = x;
+  p.ld_resid = m->cfg.hidden;
+  p.gnext = gnext;
+  p.xg_out = xg;
+  p.ld_xg = m->cfg.hidden;
+  p.ssq_out = ssq;
+  p.ssq_ld = m->cfg.hidden / kTileN;
+}
+
+// One decoder-layer stack pass.  On entry b.x holds the residual stream,
+// b.a its first-norm input bf16(x * in_norm[0]) (+ context rows after the
+// block rows for the drafter) and b.ssq_a the row sums of squares.  Every
+// RMSNorm is folded into the GEMM epilogues (see GemmParams::ssq_in).
+// On exit b.a2 / b.ssq_a2 hold the final-norm input for the LM head.
 int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
               const int32_t* pos0, const dflash_kv* kv, int ctx_rows, const int32_t* ctx_req,
               const int32_t* ctx_pos, const int32_t* tap_slot, int n_taps, uint16_t* taps,
@@ -276,18 +303,13 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
   const int H = c.hidden;
   const int max_keys = kv->max_pages * c.page_size;
   for (int l = 0; l < c.n_layers; ++l) {
-    if (l > 0) {
-      uint16_t* raw = nullptr;
-      if (taps != nullptr && tap_slot[l - 1] >= 0) raw = taps + static_cast<size_t>(tap_slot[l - 1]) * H;
-      DF_CUDA(rmsnorm_launch(b.x, rows, H, u16(m->w.in_norm) + static_cast<size_t>(l) * H,
-                             c.rms_eps, b.a, H, raw, n_taps * H, s, true));
-    }
     // QKV (+ context K/V rows in the same weight pass)
     {
       const int M = rows + ctx_rows;
       GemmParams p = gemm_base(m, M, m->qkv_rows, H, gemm_bn_for(M), ws);
       p.w_row0 = l * m->qkv_rows;
       p.mode = EPI_QKV;
+      set_norm_in(m, p, b.ssq_a, rows);
       QkvEpi e = qkv_base(m, l);
       set_pool(m, e, kv, l);
       e.q = b.q;
@@ -337,13 +359,11 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       a.status = ws.status();
       DF_CUDA(attention_launch(a, s, true));
     }
-    // O projection + residual (+ DFlash-2 block conv)
+    // O projection + residual (+ DFlash-2 block conv) -> post-norm input
     {
       GemmParams p = gemm_base(m, rows, H, m->q_dim, gemm_bn_for(rows), ws);
       p.w_row0 = l * H;
-      p.mode = EPI_RESID;
-      p.resid = b.x;
-      p.ld_resid = H;
+      set_resid_out(m, p, b.x, u16(m->w.post_norm) + static_cast<size_t>(l) * H, b.a2, b.ssq_a2);
       if (m->is_draft && c.conv_width > 0 && m->w.conv != nullptr) {
         p.conv = u16(m->w.conv) + static_cast<size_t>(l) * H * c.conv_width;
         p.conv_width = c.conv_width;
@@ -352,8 +372,6 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       int rc = run_gemm(m, &m->m_wo, b.o, m->q_dim, p, b.partial, s);
       if (rc) return rc;
     }
-    DF_CUDA(rmsnorm_launch(b.x, rows, H, u16(m->w.post_norm) + static_cast<size_t>(l) * H,
-                           c.rms_eps, b.a2, H, nullptr, 0, s, true));
     // gate/up + SwiGLU: each 128-row tile = 64 gate rows + the matching 64 up rows
     {
       GemmParams p = gemm_base(m, rows, 2 * c.mlp, H, gemm_bn_for(rows), ws);
@@ -363,26 +381,26 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       p.mode = EPI_SWIGLU;
       p.out = b.hmid;
       p.ld_out = c.mlp;
+      set_norm_in(m, p, b.ssq_a2, rows);
       int rc = run_gemm(m, &m->m_gu, b.a2, H, p, b.partial, s);
       if (rc) return rc;
     }
-    // down projection + residual
+    // down projection + residual -> next layer's in-norm input (or final norm)
     {
       GemmParams p = gemm_base(m, rows, H, c.mlp, gemm_bn_for(rows), ws);
       p.w_row0 = l * H;
-      p.mode = EPI_RESID;
-      p.resid = b.x;
-      p.ld_resid = H;
+      const bool last = (l == c.n_layers - 1);
+      const uint16_t* g = last ? u16(m->w.final_norm)
+                               : u16(m->w.in_norm) + static_cast<size_t>(l + 1) * H;
+      set_resid_out(m, p, b.x, g, last ? b.a2 : b.a, last ? b.ssq_a2 : b.ssq_a);
+      if (taps != nullptr && tap_slot[l] >= 0) {
+        p.raw_out = taps + static_cast<size_t>(tap_slot[l]) * H;
+        p.ld_raw = n_taps * H;
+      }
       int rc = run_gemm(m, &m->m_down, b.hmid, c.mlp, p, b.partial, s);
       if (rc) return rc;
     }
   }
-  // final norm (+ tap of the last layer)
-  uint16_t* raw = nullptr;
-  if (taps != nullptr && tap_slot[c.n_layers - 1] >= 0)
-    raw = taps + static_cast<size_t>(tap_slot[c.n_layers - 1]) * H;
-  DF_CUDA(rmsnorm_launch(b.x, rows, H, u16(m->w.final_norm), c.rms_eps, b.a2, H, raw, n_taps * H,
-                         s, true));
   return DFLASH_OK;
 }
 
@@ -395,6 +413,7 @@ int run_lm_head(const dflash_model_s* m, Ws& ws, StackBufs& b, int rows, int blo
   p.amax_idx = b.amax_idx;
   p.logits = logits;
   p.ld_logits = c.vocab;
+  if (b.ssq_a2 != nullptr) set_norm_in(m, p, b.ssq_a2, rows);
   p.splits = 1;  // argmax needs the full dot product per tile
   p.kb_per_split = p.kb_total;
   int rc = run_gemm(m, &m->m_lm, b.a2, c.hidden, p, b.partial, s);
@@ -650,7 +669,7 @@ int dflash_draft_block(dflash_model m, const int32_t* anchor, const int32_t* anc
   layout_stack(m, w, b, batch, B, T, max_keys);
   if (w.off > ws_bytes) return DFLASH_ERR_CAPACITY;
   DF_CUDA(embed_block_launch(anchor, batch, B, u16(m->w.embed), u16(m->w.mask_embed),
-                             u16(m->w.in_norm), c.rms_eps, c.hidden, b.x, b.a, c.hidden,
+                             u16(m->w.in_norm), c.hidden, b.x, b.a, c.hidden, b.ssq_a,
                              u16(pending_ctx), T, s, true, w.status(), c.vocab));
   rc = run_stack(m, w, b, batch, B, anchor_pos, kv, T, pending_req, pending_pos, nullptr, 0,
                  nullptr, s);
@@ -723,8 +742,8 @@ int dflash_target_forward(dflash_model m, const int32_t* tokens, const int32_t* 
   StackBufs b;
   layout_stack(m, w, b, batch, n, 0, kv->max_pages * c.page_size);
   if (w.off > ws_bytes) return DFLASH_ERR_CAPACITY;
-  DF_CUDA(embed_tokens_launch(tokens, rows, u16(m->w.embed), u16(m->w.in_norm), c.rms_eps,
-                              c.hidden, b.x, b.a, s, true, w.status(), c.vocab));
+  DF_CUDA(embed_tokens_launch(tokens, rows, u16(m->w.embed), u16(m->w.in_norm), c.hidden, b.x,
+                              b.a, b.ssq_a, s, true, w.status(), c.vocab));
   rc = run_stack(m, w, b, batch, n, pos0, kv, 0, nullptr, nullptr, slot.data(), n_taps,
                  static_cast<uint16_t*>(taps), s);
   if (rc) return rc;

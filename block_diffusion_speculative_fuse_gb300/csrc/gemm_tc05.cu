@@ -36,7 +36,7 @@ struct GemmCfg {
   static constexpr int TILE_BYTES = BN * TS_LD * 4;
   static constexpr int PIPE_BYTES = STAGES * STAGE_BYTES;
   static constexpr int MAIN_BYTES = PIPE_BYTES > TILE_BYTES ? PIPE_BYTES : TILE_BYTES;
-  static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + 1024;
+  static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + 1024 + 1024;  // + barriers, align, rinv
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
 };
 
@@ -82,35 +82,63 @@ __device__ void epi_store(const GemmParams& p, const float* ts, int tile, int m0
 template <int BN>
 __device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int rows) {
   using C = GemmCfg<BN>;
-  const int n0 = tile * kTileN;
-  if (p.conv == nullptr || p.conv_width <= 0) {
-    for (int idx = threadIdx.x; idx < rows * kTileN; idx += 128) {
-      const int r = idx / kTileN, f = idx % kTileN;
-      float* x = p.resid + static_cast<size_t>(m0 + r) * p.ld_resid + n0 + f;
-      *x += ts[r * C::TS_LD + f];
+  // Thread f owns feature column n0 + f: x_new = x + acc, then the optional
+  // depthwise conv along block positions (sliding window down the column,
+  // zero padded at each request's block edges), then the next norm's inputs.
+  const int f = threadIdx.x;
+  const int n = tile * kTileN + f;
+  for (int r = 0; r < rows; ++r)
+    ts[r * C::TS_LD + f] += p.resid[static_cast<size_t>(m0 + r) * p.ld_resid + n];
+  if (p.conv != nullptr && p.conv_width > 0) {
+    const int c = (p.conv_width - 1) / 2;
+    float w[7];
+#pragma unroll
+    for (int j = 0; j < 7; ++j) w[j] = j < p.conv_width ? bf2f(p.conv[static_cast<size_t>(n) * p.conv_width + j]) : 0.f;
+    for (int r0 = 0; r0 < rows; r0 += p.block) {
+      float win[7];  // original values x_{i-c} .. x_{i+c} of the current position
+#pragma unroll
+      for (int j = 0; j < 7; ++j) {
+        const int src = j - c;
+        win[j] = (j < p.conv_width && src >= 0 && src < p.block) ? ts[(r0 + src) * C::TS_LD + f] : 0.f;
+      }
+      for (int i = 0; i < p.block; ++i) {
+        float y = win[c];
+#pragma unroll
+        for (int j = 0; j < 7; ++j)
+          if (j < p.conv_width) y = fmaf(w[j], win[j], y);
+        // slide: drop win[0], append x_{i+1+c}
+#pragma unroll
+        for (int j = 0; j < 6; ++j) win[j] = win[j + 1];
+        const int nxt = i + 1 + c;
+        if (p.conv_width > 0) {
+          const float v = (nxt < p.block) ? ts[(r0 + nxt) * C::TS_LD + f] : 0.f;
+          // window length is conv_width; keep the slot after the last live one
+          win[p.conv_width - 1] = v;
+        }
+        ts[(r0 + i) * C::TS_LD + f] = y;
+      }
     }
-    return;
   }
-  // x_new = x + acc, then x_new += depthwise conv over the block positions
-  // of each request (zero padded), all inside this tile.
-  for (int idx = threadIdx.x; idx < rows * kTileN; idx += 128) {
-    const int r = idx / kTileN, f = idx % kTileN;
-    ts[r * C::TS_LD + f] += p.resid[static_cast<size_t>(m0 + r) * p.ld_resid + n0 + f];
+  for (int r = 0; r < rows; ++r) {
+    const float x = ts[r * C::TS_LD + f];
+    const size_t m = static_cast<size_t>(m0 + r);
+    p.resid[m * p.ld_resid + n] = x;
+    if (p.xg_out != nullptr) p.xg_out[m * p.ld_xg + n] = f2bf(x * bf2f(p.gnext[n]));
+    if (p.raw_out != nullptr) p.raw_out[m * p.ld_raw + n] = f2bf(x);
   }
-  __syncthreads();
-  const int c = (p.conv_width - 1) / 2;
-  for (int idx = threadIdx.x; idx < rows * kTileN; idx += 128) {
-    const int r = idx / kTileN, f = idx % kTileN;
-    const int i = (m0 + r) % p.block;
-    const int rbase = r - i;
-    float y = ts[r * C::TS_LD + f];
-    const uint16_t* w = p.conv + static_cast<size_t>(n0 + f) * p.conv_width;
-    for (int j = 0; j < p.conv_width; ++j) {
-      const int src = i + j - c;
-      if (src >= 0 && src < p.block && rbase + src < rows)
-        y = fmaf(bf2f(w[j]), ts[(rbase + src) * C::TS_LD + f], y);
+  if (p.ssq_out != nullptr) {
+    __syncthreads();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int r = warp; r < rows; r += 4) {
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float v = ts[r * C::TS_LD + lane + 32 * k];
+        ss = fmaf(v, v, ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) p.ssq_out[static_cast<size_t>(m0 + r) * p.ssq_ld + tile] = ss;
     }
-    p.resid[static_cast<size_t>(m0 + r) * p.ld_resid + n0 + f] = y;
   }
 }
 
@@ -393,11 +421,30 @@ __global__ void __launch_bounds__(128, 1)
       __syncthreads();
       if (*last_flag) {
         __threadfence();
-        for (int r = 0; r < rows; ++r) {
-          float s = 0.f;
-          for (int sp = 0; sp < p.splits; ++sp)
-            s += __ldcg(p.partial + (static_cast<size_t>(sp) * p.M + m0 + r) * p.N + n0 + tid);
-          ts[r * C::TS_LD + tid] = s;
+        // Sum the split partials in split order.  Each thread owns float4
+        // chunks of the tile; all loads of a group of splits are issued
+        // before they are added, so the reduction costs a few L2 round trips.
+        const size_t sstride = static_cast<size_t>(p.M) * p.N / 4;  // float4 per split
+        const float4* pbase = reinterpret_cast<const float4*>(p.partial);
+        for (int c = tid; c < rows * 32; c += 128) {
+          const int r = c / 32, c4 = c % 32;
+          const float4* src = pbase + (static_cast<size_t>(m0 + r) * p.N + n0) / 4 + c4;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          int sp = 0;
+          for (; sp + 8 <= p.splits; sp += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (sp + j) * sstride);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
+            }
+          }
+          for (; sp < p.splits; ++sp) {
+            const float4 v = __ldcg(src + sp * sstride);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+          }
+          *reinterpret_cast<float4*>(ts + r * C::TS_LD + c4 * 4) = acc;
         }
         if (tid == 0) p.counters[mt * gridDim.x + tile] = 0;
         do_epi = true;
@@ -414,6 +461,21 @@ __global__ void __launch_bounds__(128, 1)
     }
   }
   __syncthreads();
+  if (do_epi && p.ssq_in != nullptr) {
+    float* rinv = reinterpret_cast<float*>(smem + C::MAIN_BYTES + 256);
+    for (int r = tid; r < rows; r += 128) {
+      float ss = 0.f;
+      const float* q = p.ssq_in + static_cast<size_t>(m0 + r) * p.ssq_in_tiles;
+      for (int t = 0; t < p.ssq_in_tiles; ++t) ss += q[t];
+      rinv[r] = (m0 + r < p.norm_rows) ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < rows * kTileN; idx += 128) {
+      const int r = idx / kTileN, f = idx % kTileN;
+      ts[r * C::TS_LD + f] *= rinv[r];
+    }
+    __syncthreads();
+  }
   if (do_epi) {
     switch (p.mode) {
       case EPI_STORE_BF16:

@@ -67,6 +67,21 @@ struct GemmParams {
   int ld_logits;
   float* amax_val;       // [M][n_tiles]
   int32_t* amax_idx;
+  // Deferred RMSNorm of the input rows: rows m < norm_rows of the result are
+  // scaled by 1/sqrt(sum_t ssq_in[m][t] / norm_dim + norm_eps) (the input
+  // operand holds bf16(x * g), the producer wrote per-tile sums of x^2).
+  const float* ssq_in;
+  int ssq_in_tiles, norm_rows, norm_dim;
+  float norm_eps;
+  // EPI_RESID outputs for the next norm: xg_out[m][n] = bf16(x_new * gnext[n]),
+  // ssq_out[m][tile] = sum over the tile of x_new^2, raw_out = bf16(x_new).
+  const uint16_t* gnext;
+  uint16_t* xg_out;
+  int ld_xg;
+  float* ssq_out;
+  int ssq_ld;
+  uint16_t* raw_out;
+  int ld_raw;
   QkvEpi qkv;
 };
 
@@ -99,13 +114,13 @@ size_t attention_part_floats(int n_splits, int rows, int hq, int d);
 
 // small kernels (small_kernels.cu)
 cudaError_t embed_block_launch(const int32_t* anchor, int batch, int block, const uint16_t* embed,
-                               const uint16_t* mask_embed, const uint16_t* norm, float eps,
-                               int hidden, float* x, uint16_t* a, int ld_a,
+                               const uint16_t* mask_embed, const uint16_t* norm, int hidden,
+                               float* x, uint16_t* a, int ld_a, float* ssq,
                                const uint16_t* pending, int T, cudaStream_t s, bool pdl,
                                int32_t* status, int vocab);
 cudaError_t embed_tokens_launch(const int32_t* tokens, int rows, const uint16_t* embed,
-                                const uint16_t* norm, float eps, int hidden, float* x,
-                                uint16_t* a, cudaStream_t s, bool pdl, int32_t* status,
+                                const uint16_t* norm, int hidden, float* x, uint16_t* a,
+                                float* ssq, cudaStream_t s, bool pdl, int32_t* status,
                                 int vocab);
 cudaError_t rmsnorm_launch(const float* x, int rows, int hidden, const uint16_t* g, float eps,
                            uint16_t* out, int ld_out, uint16_t* raw_out, int ld_raw,

@@ -52,15 +52,37 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-// x[r] = E[anchor] (block position 0) or mask_embed (positions 1..B-1);
-// a[r] = bf16(RMSNorm(x[r]) * g).  Blocks past the block rows copy the
-// pending context rows into a[n_blk + t] so the first QKV GEMM sees
-// [block rows ; context rows] as one operand.
+// Per-row prologue of a layer stack: x[r] = float(src row), xg[r] =
+// bf16(x[r] * g) and ssq[r][t] = sum of x^2 over the 128-column tile t (the
+// next GEMM applies 1/rms per row).
+__device__ __forceinline__ void row_prologue(const uint16_t* src, const uint16_t* g, int H,
+                                             float* x, uint16_t* xg, float* ssq) {
+  for (int c = threadIdx.x; c < H; c += blockDim.x) {
+    const float v = bf2f(src[c]);
+    x[c] = v;
+    xg[c] = f2bf(v * bf2f(g[c]));
+  }
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
+  for (int t = warp; t < H / 128; t += nw) {
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float v = bf2f(src[t * 128 + lane + 32 * k]);
+      ss = fmaf(v, v, ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) ssq[t] = ss;
+  }
+}
+
+// Block rows: E[anchor] at block position 0, mask_embed at 1..B-1.  Blocks
+// past the block rows copy the pending context rows into a[n_blk + t] so the
+// first QKV GEMM sees [block rows ; context rows] as one operand.
 __global__ void __launch_bounds__(kRowThreads)
     embed_block_kernel(const int32_t* anchor, int block, int n_blk, const uint16_t* embed,
-                       const uint16_t* mask_embed, const uint16_t* g, float eps, int H, float* x,
-                       uint16_t* a, int ld_a, const uint16_t* pending, int32_t* status, int vocab) {
-  __shared__ float red[32];
+                       const uint16_t* mask_embed, const uint16_t* g, int H, float* x,
+                       uint16_t* a, int ld_a, float* ssq, const uint16_t* pending,
+                       int32_t* status, int vocab) {
   griddep_launch_dependents();
   griddep_wait();
   const int r = blockIdx.x;
@@ -80,22 +102,13 @@ __global__ void __launch_bounds__(kRowThreads)
     }
     src = embed + static_cast<size_t>(tok) * H;
   }
-  float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = bf2f(src[c]);
-    x[static_cast<size_t>(r) * H + c] = v;
-    ss += v * v;
-  }
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
-  for (int c = threadIdx.x; c < H; c += blockDim.x)
-    a[static_cast<size_t>(r) * ld_a + c] = f2bf(bf2f(src[c]) * inv * bf2f(g[c]));
+  row_prologue(src, g, H, x + static_cast<size_t>(r) * H, a + static_cast<size_t>(r) * ld_a,
+               ssq + static_cast<size_t>(r) * (H / 128));
 }
 
 __global__ void __launch_bounds__(kRowThreads)
-    embed_tokens_kernel(const int32_t* tokens, const uint16_t* embed, const uint16_t* g, float eps,
-                        int H, float* x, uint16_t* a, int32_t* status, int vocab) {
-  __shared__ float red[32];
+    embed_tokens_kernel(const int32_t* tokens, const uint16_t* embed, const uint16_t* g, int H,
+                        float* x, uint16_t* a, float* ssq, int32_t* status, int vocab) {
   griddep_launch_dependents();
   griddep_wait();
   const int r = blockIdx.x;
@@ -104,17 +117,8 @@ __global__ void __launch_bounds__(kRowThreads)
     if (threadIdx.x == 0) raise_status(status, DFLASH_ERR_INVALID_ARG, 302);
     tok = 0;
   }
-  const uint16_t* src = embed + static_cast<size_t>(tok) * H;
-  float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = bf2f(src[c]);
-    x[static_cast<size_t>(r) * H + c] = v;
-    ss += v * v;
-  }
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
-  for (int c = threadIdx.x; c < H; c += blockDim.x)
-    a[static_cast<size_t>(r) * H + c] = f2bf(bf2f(src[c]) * inv * bf2f(g[c]));
+  row_prologue(embed + static_cast<size_t>(tok) * H, g, H, x + static_cast<size_t>(r) * H,
+               a + static_cast<size_t>(r) * H, ssq + static_cast<size_t>(r) * (H / 128));
 }
 
 // out[r] = bf16(x[r] * g / sqrt(mean(x[r]^2) + eps)); raw_out[r] = bf16(x[r]).
@@ -256,20 +260,20 @@ __global__ void copy_f32_kernel(const float* src, float* dst, size_t n) {
 
 // ---------------------------------------------------------------- launchers
 cudaError_t embed_block_launch(const int32_t* anchor, int batch, int block, const uint16_t* embed,
-                               const uint16_t* mask_embed, const uint16_t* norm, float eps,
-                               int hidden, float* x, uint16_t* a, int ld_a,
+                               const uint16_t* mask_embed, const uint16_t* norm, int hidden,
+                               float* x, uint16_t* a, int ld_a, float* ssq,
                                const uint16_t* pending, int T, cudaStream_t s, bool pdl,
                                int32_t* status, int vocab) {
   const int nb = batch * block;
   return launch(embed_block_kernel, dim3(nb + T), dim3(kRowThreads), 0, s, pdl, anchor, block, nb,
-                embed, mask_embed, norm, eps, hidden, x, a, ld_a, pending, status, vocab);
+                embed, mask_embed, norm, hidden, x, a, ld_a, ssq, pending, status, vocab);
 }
 cudaError_t embed_tokens_launch(const int32_t* tokens, int rows, const uint16_t* embed,
-                                const uint16_t* norm, float eps, int hidden, float* x,
-                                uint16_t* a, cudaStream_t s, bool pdl, int32_t* status,
+                                const uint16_t* norm, int hidden, float* x, uint16_t* a,
+                                float* ssq, cudaStream_t s, bool pdl, int32_t* status,
                                 int vocab) {
   return launch(embed_tokens_kernel, dim3(rows), dim3(kRowThreads), 0, s, pdl, tokens, embed, norm,
-                eps, hidden, x, a, status, vocab);
+                hidden, x, a, ssq, status, vocab);
 }
 cudaError_t rmsnorm_launch(const float* x, int rows, int hidden, const uint16_t* g, float eps,
                            uint16_t* out, int ld_out, uint16_t* raw_out, int ld_raw,

@@ -1,0 +1,111 @@
+"""End-to-end greedy speculative decoding on the GPU (causal target path).
+
+Losslessness: GPU speculative output == GPU autoregressive output, token for
+token (the target path is batch invariant).  Against the oracle: target
+logits within 0.05 and tapped states within 2e-2 (relative row norm); tokens
+equal up to the first position where the oracle's top-1/top-2 gap is <= 0.1.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workload as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_diffusion_speculative_fuse_gb300 import _build, binding
+    _build.build()
+    binding.load()
+
+
+def models(wl, target_std=0.02):
+    from block_diffusion_speculative_fuse_gb300.device import DeviceModel
+    ts, ds = wl.target, wl.draft
+    shared = W.shared_weights(ts, wl.wid, std=target_std)
+    tw = W.target_weights(ts, wl.wid, std=target_std)
+    dw = W.draft_weights(ds, wl.wid)
+    tm = DeviceModel(ts, tw, shared, draft=False)
+    dm = DeviceModel(ds, dw, {k: tm.t[k] for k in ("embed", "lm_head")}, draft=True)
+    return shared, tw, dw, tm, dm
+
+
+def test_target_forward_parity_and_taps_tiny():
+    from block_diffusion_speculative_fuse_gb300.device import i32
+    from block_diffusion_speculative_fuse_gb300.generate import TargetRunner
+    wl = W.get_workload("tiny_e2e")
+    shared, tw, dw, tm, dm = models(wl, target_std=0.05)
+    P = 40
+    prompt = W.uniform_tokens(P, wl.target.vocab, wl.wid, W.TENSOR_IDS["prompt"])
+    run = TargetRunner(tm, 1, 128, P, wl.tap_layers)
+    logits = torch.zeros((P, wl.target.vocab), dtype=torch.float32, device="cuda")
+    out, taps = run.forward(i32(prompt[None]), i32([0]), P, want_taps=True, logits=logits)
+    torch.cuda.synchronize()
+    tws = O.LayerStack(wl.target, tw, shared)
+    cache = O.TargetCache(wl.target, 128)
+    lref, href = O.target_rows(wl.target, tws, prompt, 0, cache, wl.tap_layers)
+    lg = logits.cpu().numpy()
+    assert np.abs(lg - lref).max() <= 0.05
+    hg = taps.float().cpu().numpy()
+    err = np.max(np.linalg.norm(hg - href, axis=1) / np.linalg.norm(href, axis=1))
+    assert err <= 2e-2, err
+    top = np.sort(lref, axis=-1)
+    sure = (top[:, -1] - top[:, -2]) > 0.1
+    assert np.array_equal(out.cpu().numpy()[0][sure], np.argmax(lref, -1)[sure])
+
+
+def _first_unsure(tokens_ref_logits):
+    for i, lg in enumerate(tokens_ref_logits):
+        top = np.sort(lg)
+        if top[-1] - top[-2] <= 0.1:
+            return i
+    return len(tokens_ref_logits)
+
+
+def test_tiny_e2e_spec_equals_ar_and_oracle():
+    """tiny_e2e: 4-layer H=256 target, 2-layer B=8 drafter, prompt 64,
+    generate 128, batch 1."""
+    from block_diffusion_speculative_fuse_gb300.generate import SpecDecoder, TargetRunner, \
+        ar_generate
+    wl = W.get_workload("tiny_e2e")
+    shared, tw, dw, tm, dm = models(wl, target_std=0.05)
+    P, N = wl.prompt_len, wl.gen_tokens
+    prompt = W.uniform_tokens(P, wl.target.vocab, wl.wid, W.TENSOR_IDS["prompt"])[None]
+    ar = ar_generate(TargetRunner(tm, 1, P + N + 1, P), prompt, N)
+    sd = SpecDecoder(tm, dm, wl.tap_layers, 1, P + N)
+    sp = sd.generate(prompt, N)
+    assert np.array_equal(sp, ar), "speculative output differs from autoregressive output"
+    assert all(0 <= n <= wl.draft.block - 1 for n in sd.stats)
+    # oracle AR, compared while the oracle's decisions are unambiguous
+    tws = O.LayerStack(wl.target, tw, shared)
+    cache = O.TargetCache(wl.target, P + N + 1)
+    lg, _ = O.target_rows(wl.target, tws, prompt[0], 0, cache)
+    ref_tokens, ref_logits = [int(np.argmax(lg[-1]))], [lg[-1]]
+    pos = P
+    while len(ref_tokens) < N:
+        l1, _ = O.target_row(wl.target, tws, ref_tokens[-1], pos, cache)
+        ref_tokens.append(int(np.argmax(l1)))
+        ref_logits.append(l1)
+        pos += 1
+    k = _first_unsure(ref_logits)
+    assert k >= 8, "the oracle decisions are ambiguous too early to compare"
+    assert np.array_equal(ar[0, :k], np.array(ref_tokens[:k]))
+
+
+@pytest.mark.parametrize("block", [1, 4])
+def test_spec_equals_ar_other_block_sizes(block):
+    from dataclasses import replace
+    from block_diffusion_speculative_fuse_gb300.generate import SpecDecoder, TargetRunner, \
+        ar_generate
+    wl = W.get_workload("tiny_e2e")
+    wl = replace(wl, draft=replace(wl.draft, block=block))
+    shared, tw, dw, tm, dm = models(wl, target_std=0.05)
+    prompt = W.uniform_tokens(2 * 24, wl.target.vocab, 3, 3).reshape(2, 24)
+    ar = ar_generate(TargetRunner(tm, 2, 24 + 40 + 1, 24), prompt, 40)
+    sd = SpecDecoder(tm, dm, wl.tap_layers, 2, 24 + 40)
+    assert np.array_equal(sd.generate(prompt, 40), ar)
