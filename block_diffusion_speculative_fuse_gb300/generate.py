@@ -35,7 +35,8 @@ class TargetRunner:
         self.batch = batch
         table, npg = _sequential_table(batch, max_len, 16)
         self.kv = PagedKV(self.shape, table, npg, 16, device)
-        self.taps_ids = i32(list(tap_layers), device) if len(tap_layers) else None
+        # host array: the library reads the layer list on the host
+        self.taps_ids = torch.tensor(list(tap_layers), dtype=torch.int32) if len(tap_layers) else None
         self.n_taps = len(tap_layers)
         self.max_len = max_len
         self.device = device

@@ -210,9 +210,10 @@ int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t ba
 /* Causal target forward over `batch` requests x `n` consecutive rows:
  * tokens int32 [batch][n], row i of request r at position pos0[r] + i.  Each
  * row's K/V are written to the target cache at its position, then each row
- * attends to positions [0, pos0[r] + i] of its request.  Outputs: argmax
+ * attends to positions [0, pos0[r] + i] of its request.  tap_layers is a
+ * HOST int32 array of n_taps distinct 0-indexed layers.  Outputs: argmax
  * int32 [batch][n]; optional taps bf16 [batch*n][n_taps*hidden] (residual
- * output of each listed 0-indexed layer, in list order); optional logits fp32
+ * output of each listed layer, in list order); optional logits fp32
  * [batch*n][vocab].  A row's results do not depend on the other rows of the
  * call (fixed split-K and key-split boundaries), so a block verify and a
  * one-token-at-a-time decode give bit-identical tokens. */
