@@ -59,14 +59,6 @@ def test_target_forward_parity_and_taps_tiny():
     assert np.array_equal(out.cpu().numpy()[0][sure], np.argmax(lref, -1)[sure])
 
 
-def _first_unsure(tokens_ref_logits):
-    for i, lg in enumerate(tokens_ref_logits):
-        top = np.sort(lg)
-        if top[-1] - top[-2] <= 0.1:
-            return i
-    return len(tokens_ref_logits)
-
-
 def test_tiny_e2e_spec_equals_ar_and_oracle():
     """tiny_e2e: 4-layer H=256 target, 2-layer B=8 drafter, prompt 64,
     generate 128, batch 1."""
@@ -81,20 +73,17 @@ def test_tiny_e2e_spec_equals_ar_and_oracle():
     sp = sd.generate(prompt, N)
     assert np.array_equal(sp, ar), "speculative output differs from autoregressive output"
     assert all(0 <= n <= wl.draft.block - 1 for n in sd.stats)
-    # oracle AR, compared while the oracle's decisions are unambiguous
+    # oracle with teacher forcing on the GPU's own sequence: at every position
+    # whose oracle top-1/top-2 gap exceeds 0.1 the GPU token is the argmax
     tws = O.LayerStack(wl.target, tw, shared)
     cache = O.TargetCache(wl.target, P + N + 1)
-    lg, _ = O.target_rows(wl.target, tws, prompt[0], 0, cache)
-    ref_tokens, ref_logits = [int(np.argmax(lg[-1]))], [lg[-1]]
-    pos = P
-    while len(ref_tokens) < N:
-        l1, _ = O.target_row(wl.target, tws, ref_tokens[-1], pos, cache)
-        ref_tokens.append(int(np.argmax(l1)))
-        ref_logits.append(l1)
-        pos += 1
-    k = _first_unsure(ref_logits)
-    assert k >= 8, "the oracle decisions are ambiguous too early to compare"
-    assert np.array_equal(ar[0, :k], np.array(ref_tokens[:k]))
+    seq = np.concatenate([prompt[0], ar[0, :-1]])
+    lg, _ = O.target_rows(wl.target, tws, seq, 0, cache)
+    lg = lg[P - 1:]
+    top = np.sort(lg, axis=-1)
+    sure = (top[:, -1] - top[:, -2]) > 0.1
+    assert sure.sum() >= N // 5, "too few unambiguous positions to compare"
+    assert np.array_equal(ar[0][sure], np.argmax(lg, -1)[sure])
 
 
 @pytest.mark.parametrize("block", [1, 4])
