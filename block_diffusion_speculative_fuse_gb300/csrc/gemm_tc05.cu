@@ -36,7 +36,7 @@ struct GemmCfg {
   static constexpr int TILE_BYTES = BN * TS_LD * 4;
   static constexpr int PIPE_BYTES = STAGES * STAGE_BYTES;
   static constexpr int MAIN_BYTES = PIPE_BYTES > TILE_BYTES ? PIPE_BYTES : TILE_BYTES;
-  static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + 1024 + 1024;  // + barriers, align, rinv
+  static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + 1024 + 3 * 1024 + 1024;  // barriers, rinv, routing, align
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
 };
 
@@ -87,8 +87,15 @@ __device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int 
   // zero padded at each request's block edges), then the next norm's inputs.
   const int f = threadIdx.x;
   const int n = tile * kTileN + f;
-  for (int r = 0; r < rows; ++r)
-    ts[r * C::TS_LD + f] += p.resid[static_cast<size_t>(m0 + r) * p.ld_resid + n];
+  for (int r0 = 0; r0 < rows; r0 += 16) {
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      v[j] = (r0 + j < rows) ? __ldcg(p.resid + static_cast<size_t>(m0 + r0 + j) * p.ld_resid + n) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (r0 + j < rows) ts[(r0 + j) * C::TS_LD + f] += v[j];
+  }
   if (p.conv != nullptr && p.conv_width > 0) {
     const int c = (p.conv_width - 1) / 2;
     float w[7];
@@ -189,7 +196,8 @@ __device__ void epi_argmax(const GemmParams& p, const float* ts, int tile, int m
 }
 
 template <int BN>
-__device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, int rows) {
+__device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, int rows,
+                        int* route) {
   using C = GemmCfg<BN>;
   const QkvEpi& e = p.qkv;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -198,15 +206,15 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
   const int per_tile = kTileN / d;
   const int npair = half / 32;  // pairs per lane: 1 (d=64) or 2 (d=128)
   const int hq = e.n_q_heads, hkv = e.n_kv_heads;
-  for (int w = warp; w < rows * per_tile; w += 4) {
-    const int r = w / per_tile, hl = w % per_tile;
+  // Per-row routing, one thread per row, all lookups issued in parallel:
+  // route[r] = (request, position, physical page or -1 for block rows / -2 skip)
+  int* r_req = route;
+  int* r_pos = route + BN;
+  int* r_pg = route + 2 * BN;
+  for (int r = threadIdx.x; r < rows; r += 128) {
     const int m = m0 + r;
-    const int head = (e.f0 + tile * kTileN + hl * d) / d;
-    const int kind = head < hq ? 0 : (head < hq + hkv ? 1 : 2);
-    const int hidx = kind == 0 ? head : (kind == 1 ? head - hq : head - hq - hkv);
-    const bool is_blk = m < e.n_blk;
-    int req, pos;
-    if (is_blk) {
+    int req, pos, pg = -1;
+    if (m < e.n_blk) {
       req = m / e.block;
       pos = e.anchor_pos[req] + m % e.block;
     } else {
@@ -218,7 +226,39 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
         req = j / e.rows_per_req;
         pos = e.pool_pos0[req] + j % e.rows_per_req;
       }
-      if (pos < 0) continue;
+      if (pos < 0) {
+        pg = -2;
+      } else {
+        const int pi = pos / e.page_size;
+        pg = pi < e.max_pages ? e.page_table[static_cast<size_t>(req) * e.max_pages + pi] : -3;
+        if (pg < 0 || pg >= e.n_pages) {
+          raise_status(p.status, DFLASH_ERR_CAPACITY, 101);
+          pg = -2;
+        }
+      }
+    }
+    r_req[r] = req;
+    r_pos[r] = pos;
+    r_pg[r] = pg;
+  }
+  float gq[4], gk[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int i = lane + 32 * t;
+    gq[t] = (e.q_norm != nullptr && i < d) ? bf2f(e.q_norm[i]) : 1.f;
+    gk[t] = (e.k_norm != nullptr && i < d) ? bf2f(e.k_norm[i]) : 1.f;
+  }
+  __syncthreads();
+  for (int w = warp; w < rows * per_tile; w += 4) {
+    const int r = w / per_tile, hl = w % per_tile;
+    const int m = m0 + r;
+    const int head = (e.f0 + tile * kTileN + hl * d) / d;
+    const int kind = head < hq ? 0 : (head < hq + hkv ? 1 : 2);
+    const int hidx = kind == 0 ? head : (kind == 1 ? head - hq : head - hq - hkv);
+    const bool is_blk = m < e.n_blk;
+    const int req = r_req[r], pos = r_pos[r], pg = r_pg[r];
+    if (!is_blk) {
+      if (pg == -2) continue;
       if (kind == 0 && !e.keep_q_pool) continue;
     }
     const float* xs = ts + r * C::TS_LD + hl * d;
@@ -231,19 +271,22 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
       }
     }
     if (kind < 2) {
-      const uint16_t* g = kind == 0 ? e.q_norm : e.k_norm;
-      if (g != nullptr) {
+      const bool norm = kind == 0 ? (e.q_norm != nullptr) : (e.k_norm != nullptr);
+      if (norm) {
         float ss = 0.f;
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           if (t < npair) ss += x1[t] * x1[t] + x2[t] * x2[t];
         ss = warp_sum(ss);
         const float inv = rsqrtf(ss / static_cast<float>(d) + e.eps);
+        // gain index lane+32t lives in slot t; its rotate-half partner in slot t + npair
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (t < npair) {
-            x1[t] = x1[t] * inv * bf2f(g[lane + 32 * t]);
-            x2[t] = x2[t] * inv * bf2f(g[lane + 32 * t + half]);
+            const float ga = kind == 0 ? gq[t] : gk[t];
+            const float gb = kind == 0 ? gq[t + npair] : gk[t + npair];
+            x1[t] = x1[t] * inv * ga;
+            x2[t] = x2[t] * inv * gb;
           }
         }
       }
@@ -265,12 +308,6 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
       dst = (kind == 1 ? e.kblk : e.vblk) +
             ((static_cast<size_t>(req) * hkv + hidx) * e.block + m % e.block) * d;
     } else {
-      const int pi = pos / e.page_size;
-      const int pg = pi < e.max_pages ? e.page_table[static_cast<size_t>(req) * e.max_pages + pi] : -1;
-      if (pg < 0 || pg >= e.n_pages) {
-        if (lane == 0) raise_status(p.status, DFLASH_ERR_CAPACITY, 101);
-        continue;
-      }
       dst = e.pool + ((((static_cast<size_t>(pg) * 2 + (kind - 1)) * hkv + hidx) * e.page_size) +
                       pos % e.page_size) * d;
     }
@@ -426,25 +463,50 @@ __global__ void __launch_bounds__(128, 1)
         // before they are added, so the reduction costs a few L2 round trips.
         const size_t sstride = static_cast<size_t>(p.M) * p.N / 4;  // float4 per split
         const float4* pbase = reinterpret_cast<const float4*>(p.partial);
-        for (int c = tid; c < rows * 32; c += 128) {
-          const int r = c / 32, c4 = c % 32;
-          const float4* src = pbase + (static_cast<size_t>(m0 + r) * p.N + n0) / 4 + c4;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int nchunk = rows * 32;  // float4 chunks of the tile
+        for (int c0 = tid; c0 < nchunk; c0 += 4 * 128) {
+          // up to 4 chunks per thread at once, splits in groups of 4: 16 loads in flight
+          const float4* src[4];
+          float4 acc[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = c0 + i * 128;
+            const int r = c / 32, c4 = c % 32;
+            src[i] = pbase + (static_cast<size_t>(m0 + (c < nchunk ? r : 0)) * p.N + n0) / 4 + c4;
+            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
           int sp = 0;
-          for (; sp + 8 <= p.splits; sp += 8) {
-            float4 v[8];
+          for (; sp + 4 <= p.splits; sp += 4) {
+            float4 v[4][4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (sp + j) * sstride);
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
-            }
+              for (int j = 0; j < 4; ++j)
+                v[i][j] = (c0 + i * 128 < nchunk) ? __ldcg(src[i] + (sp + j) * sstride)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                acc[i].x += v[i][j].x; acc[i].y += v[i][j].y;
+                acc[i].z += v[i][j].z; acc[i].w += v[i][j].w;
+              }
           }
           for (; sp < p.splits; ++sp) {
-            const float4 v = __ldcg(src + sp * sstride);
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (c0 + i * 128 < nchunk) {
+                const float4 v = __ldcg(src[i] + sp * sstride);
+                acc[i].x += v.x; acc[i].y += v.y; acc[i].z += v.z; acc[i].w += v.w;
+              }
+            }
           }
-          *reinterpret_cast<float4*>(ts + r * C::TS_LD + c4 * 4) = acc;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = c0 + i * 128;
+            if (c < nchunk)
+              *reinterpret_cast<float4*>(ts + (c / 32) * C::TS_LD + (c % 32) * 4) = acc[i];
+          }
         }
         if (tid == 0) p.counters[mt * gridDim.x + tile] = 0;
         do_epi = true;
@@ -462,12 +524,16 @@ __global__ void __launch_bounds__(128, 1)
   }
   __syncthreads();
   if (do_epi && p.ssq_in != nullptr) {
+    // one warp per row: the lanes read the row's per-tile sums together and
+    // combine them with a fixed butterfly (same order for any M)
     float* rinv = reinterpret_cast<float*>(smem + C::MAIN_BYTES + 256);
-    for (int r = tid; r < rows; r += 128) {
-      float ss = 0.f;
+    for (int r = warp; r < rows; r += 4) {
       const float* q = p.ssq_in + static_cast<size_t>(m0 + r) * p.ssq_in_tiles;
-      for (int t = 0; t < p.ssq_in_tiles; ++t) ss += q[t];
-      rinv[r] = (m0 + r < p.norm_rows) ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
+      float ss = 0.f;
+      for (int t = lane; t < p.ssq_in_tiles; t += 32) ss += q[t];
+      ss = warp_sum(ss);
+      if (lane == 0)
+        rinv[r] = (m0 + r < p.norm_rows) ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
     }
     __syncthreads();
     for (int idx = tid; idx < rows * kTileN; idx += 128) {
@@ -483,7 +549,9 @@ __global__ void __launch_bounds__(128, 1)
       case EPI_RESID: epi_resid<BN>(p, ts, tile, m0, rows); break;
       case EPI_SWIGLU: epi_swiglu<BN>(p, ts, tile, m0, rows); break;
       case EPI_ARGMAX: epi_argmax<BN>(p, ts, tile, m0, rows); break;
-      case EPI_QKV: epi_qkv<BN>(p, ts, tile, m0, rows); break;
+      case EPI_QKV:
+        epi_qkv<BN>(p, ts, tile, m0, rows, reinterpret_cast<int*>(smem + C::MAIN_BYTES + 256 + 1024));
+        break;
       default: break;
     }
   }
