@@ -36,7 +36,10 @@ struct GemmCfg {
   static constexpr int TILE_BYTES = BN * TS_LD * 4;
   static constexpr int PIPE_BYTES = STAGES * STAGE_BYTES;
   static constexpr int MAIN_BYTES = PIPE_BYTES > TILE_BYTES ? PIPE_BYTES : TILE_BYTES;
-  static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + 1024 + 3 * 1024 + 1024;  // barriers, rinv, routing, align
+  // epilogue scratch (row scales, QKV routing) sits after the staged tile
+  static constexpr int SCRATCH_OFF = (TILE_BYTES + 255) / 256 * 256;
+  static_assert(SCRATCH_OFF + 4 * BN * 4 <= MAIN_BYTES, "epilogue scratch must fit the pipeline region");
+  static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + 1024;  // + barriers, alignment slack
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
 };
 
@@ -526,7 +529,7 @@ __global__ void __launch_bounds__(128, 1)
   if (do_epi && p.ssq_in != nullptr) {
     // one warp per row: the lanes read the row's per-tile sums together and
     // combine them with a fixed butterfly (same order for any M)
-    float* rinv = reinterpret_cast<float*>(smem + C::MAIN_BYTES + 256);
+    float* rinv = reinterpret_cast<float*>(smem + C::SCRATCH_OFF);
     for (int r = warp; r < rows; r += 4) {
       const float* q = p.ssq_in + static_cast<size_t>(m0 + r) * p.ssq_in_tiles;
       float ss = 0.f;
@@ -550,7 +553,7 @@ __global__ void __launch_bounds__(128, 1)
       case EPI_SWIGLU: epi_swiglu<BN>(p, ts, tile, m0, rows); break;
       case EPI_ARGMAX: epi_argmax<BN>(p, ts, tile, m0, rows); break;
       case EPI_QKV:
-        epi_qkv<BN>(p, ts, tile, m0, rows, reinterpret_cast<int*>(smem + C::MAIN_BYTES + 256 + 1024));
+        epi_qkv<BN>(p, ts, tile, m0, rows, reinterpret_cast<int*>(smem + C::SCRATCH_OFF + BN * 4));
         break;
       default: break;
     }
