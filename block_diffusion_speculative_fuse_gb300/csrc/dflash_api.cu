@@ -84,6 +84,7 @@ namespace {
 constexpr size_t kHeaderBytes = 64 * 1024;       // status word + split counters
 constexpr int kMaxCounters = (kHeaderBytes - 256) / 4;
 constexpr int kTargetSplitKeys = 512;
+constexpr int kMaxClusterSplits = 8;  // portable cluster size
 
 size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -98,7 +99,7 @@ int choose_splits(const dflash_model_s* m, int n_tiles, int m_tiles, int kb_tota
   const int base = n_tiles * (m->is_draft ? m_tiles : 1);
   int s = capacity / std::max(1, base);
   s = std::max(1, std::min(s, kb_total / 2));
-  s = std::min(s, 32);
+  s = std::min(s, kMaxClusterSplits);  // the splits of a tile form one thread-block cluster
   return s;
 }
 

@@ -439,82 +439,12 @@ __global__ void __launch_bounds__(128, 1)
   const int f = warp * 32 + lane;
   const int n0 = tile * kTileN;
   bool do_epi = false;
-  if (!aborted) {
-    if (p.splits > 1) {
-      float* part = p.partial + static_cast<size_t>(split) * p.M * p.N;
-#pragma unroll 1
-      for (int c = 0; c < BN / 16; ++c) {
-        float v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 16, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = c * 16 + j;
-          if (r < rows) part[static_cast<size_t>(m0 + r) * p.N + n0 + f] = v[j];
-        }
-      }
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) {
-        const int prev = atomicAdd(&p.counters[mt * gridDim.x + tile], 1);
-        *last_flag = (prev == p.splits - 1) ? 1 : 0;
-      }
-      __syncthreads();
-      if (*last_flag) {
-        __threadfence();
-        // Sum the split partials in split order.  Each thread owns float4
-        // chunks of the tile; all loads of a group of splits are issued
-        // before they are added, so the reduction costs a few L2 round trips.
-        const size_t sstride = static_cast<size_t>(p.M) * p.N / 4;  // float4 per split
-        const float4* pbase = reinterpret_cast<const float4*>(p.partial);
-        const int nchunk = rows * 32;  // float4 chunks of the tile
-        for (int c0 = tid; c0 < nchunk; c0 += 4 * 128) {
-          // up to 4 chunks per thread at once, splits in groups of 4: 16 loads in flight
-          const float4* src[4];
-          float4 acc[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = c0 + i * 128;
-            const int r = c / 32, c4 = c % 32;
-            src[i] = pbase + (static_cast<size_t>(m0 + (c < nchunk ? r : 0)) * p.N + n0) / 4 + c4;
-            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-          int sp = 0;
-          for (; sp + 4 <= p.splits; sp += 4) {
-            float4 v[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                v[i][j] = (c0 + i * 128 < nchunk) ? __ldcg(src[i] + (sp + j) * sstride)
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                acc[i].x += v[i][j].x; acc[i].y += v[i][j].y;
-                acc[i].z += v[i][j].z; acc[i].w += v[i][j].w;
-              }
-          }
-          for (; sp < p.splits; ++sp) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (c0 + i * 128 < nchunk) {
-                const float4 v = __ldcg(src[i] + sp * sstride);
-                acc[i].x += v.x; acc[i].y += v.y; acc[i].z += v.z; acc[i].w += v.w;
-              }
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = c0 + i * 128;
-            if (c < nchunk)
-              *reinterpret_cast<float4*>(ts + (c / 32) * C::TS_LD + (c % 32) * 4) = acc[i];
-          }
-        }
-        if (tid == 0) p.counters[mt * gridDim.x + tile] = 0;
-        do_epi = true;
-      }
-    } else {
+  // rows of the tile this CTA finishes: all of them without split-K; with
+  // split-K the S CTAs of the tile form one cluster and CTA q finishes rows
+  // [q*rpc, q*rpc + rpc) (request-aligned when the block conv couples rows)
+  int r_beg = 0, r_cnt = rows;
+  if (p.splits == 1) {
+    if (!aborted) {
 #pragma unroll 1
       for (int c = 0; c < BN / 16; ++c) {
         float v[16];
@@ -524,40 +454,97 @@ __global__ void __launch_bounds__(128, 1)
       }
       do_epi = true;
     }
+  } else {
+    // 1) own partial tile -> own shared memory
+    if (!aborted) {
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 16, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ts[(c * 16 + j) * C::TS_LD + f] = v[j];
+      }
+    }
+    cluster_sync();
+    // 2) reduce this CTA's rows over the cluster's partials (split order)
+    const int S = p.splits;
+    const int q = static_cast<int>(cluster_ctarank());
+    int rpc = (rows + S - 1) / S;
+    if (p.conv != nullptr && p.conv_width > 0) rpc = (rpc + p.block - 1) / p.block * p.block;
+    r_beg = min(rows, q * rpc);
+    r_cnt = min(rows, r_beg + rpc) - r_beg;
+    // Peers read only rows of their own range from this CTA's tile and this
+    // CTA overwrites only rows of its range, so the in-place write needs no
+    // extra barrier; the final cluster barrier keeps every tile alive until
+    // all peers are done reading.
+    const uint32_t ts_addr = smem_u32(ts);
+    const int nchunk = r_cnt * 32;  // float4 chunks of my rows
+    for (int c0 = tid; c0 < nchunk; c0 += 4 * 128) {
+      float4 red[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) red[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int sp = 0; sp < S; ++sp) {
+        const uint32_t peer = dsmem_map(ts_addr, static_cast<uint32_t>(sp));
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = c0 + i * 128;
+          v[i] = c < nchunk
+                     ? dsmem_ld4(peer + static_cast<uint32_t>(((r_beg + c / 32) * C::TS_LD + (c % 32) * 4) * 4))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          red[i].x += v[i].x; red[i].y += v[i].y; red[i].z += v[i].z; red[i].w += v[i].w;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = c0 + i * 128;
+        if (c < nchunk)
+          *reinterpret_cast<float4*>(ts + (r_beg + c / 32) * C::TS_LD + (c % 32) * 4) = red[i];
+      }
+    }
+    __syncthreads();
+    do_epi = !aborted && r_cnt > 0;
   }
-  __syncthreads();
+  float* tsv = ts + r_beg * C::TS_LD;   // first row this CTA finishes
+  const int m0v = m0 + r_beg;
+  const int rows_v = r_cnt;
   if (do_epi && p.ssq_in != nullptr) {
     // one warp per row: the lanes read the row's per-tile sums together and
     // combine them with a fixed butterfly (same order for any M)
     float* rinv = reinterpret_cast<float*>(smem + C::SCRATCH_OFF);
-    for (int r = warp; r < rows; r += 4) {
-      const float* q = p.ssq_in + static_cast<size_t>(m0 + r) * p.ssq_in_tiles;
+    for (int r = warp; r < rows_v; r += 4) {
+      const float* q = p.ssq_in + static_cast<size_t>(m0v + r) * p.ssq_in_tiles;
       float ss = 0.f;
       for (int t = lane; t < p.ssq_in_tiles; t += 32) ss += q[t];
       ss = warp_sum(ss);
       if (lane == 0)
-        rinv[r] = (m0 + r < p.norm_rows) ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
+        rinv[r] = (m0v + r < p.norm_rows) ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
     }
     __syncthreads();
-    for (int idx = tid; idx < rows * kTileN; idx += 128) {
+    for (int idx = tid; idx < rows_v * kTileN; idx += 128) {
       const int r = idx / kTileN, f = idx % kTileN;
-      ts[r * C::TS_LD + f] *= rinv[r];
+      tsv[r * C::TS_LD + f] *= rinv[r];
     }
     __syncthreads();
   }
   if (do_epi) {
     switch (p.mode) {
       case EPI_STORE_BF16:
-      case EPI_STORE_F32: epi_store<BN>(p, ts, tile, m0, rows); break;
-      case EPI_RESID: epi_resid<BN>(p, ts, tile, m0, rows); break;
-      case EPI_SWIGLU: epi_swiglu<BN>(p, ts, tile, m0, rows); break;
-      case EPI_ARGMAX: epi_argmax<BN>(p, ts, tile, m0, rows); break;
+      case EPI_STORE_F32: epi_store<BN>(p, tsv, tile, m0v, rows_v); break;
+      case EPI_RESID: epi_resid<BN>(p, tsv, tile, m0v, rows_v); break;
+      case EPI_SWIGLU: epi_swiglu<BN>(p, tsv, tile, m0v, rows_v); break;
+      case EPI_ARGMAX: epi_argmax<BN>(p, tsv, tile, m0v, rows_v); break;
       case EPI_QKV:
-        epi_qkv<BN>(p, ts, tile, m0, rows, reinterpret_cast<int*>(smem + C::SCRATCH_OFF + BN * 4));
+        epi_qkv<BN>(p, tsv, tile, m0v, rows_v, reinterpret_cast<int*>(smem + C::SCRATCH_OFF + BN * 4));
         break;
       default: break;
     }
   }
+  if (p.splits > 1) cluster_sync();  // peers may still read this CTA's tile until here
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
@@ -595,11 +582,23 @@ static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (p.splits > 1) {
+    // the split-K CTAs of one output tile form a cluster (reduced through DSMEM)
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = p.splits;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   count_launch();
   return cudaLaunchKernelEx(&cfg, gemm_tc05_kernel<BN>, *w_map, *x_map, p);
 }
