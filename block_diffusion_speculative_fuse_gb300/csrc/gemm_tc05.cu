@@ -28,7 +28,10 @@ namespace dflash {
 
 template <int BN>
 struct GemmCfg {
-  static constexpr int STAGES = BN <= 16 ? 6 : BN <= 32 ? 5 : BN <= 64 ? 4 : BN <= 128 ? 6 : 4;
+  // BN <= 32 (decode-sized M): 3 CTAs fit per SM, so while a GEMM runs on two
+  // slots the next kernel's CTAs (programmatic dependent launch) occupy the
+  // third and prefetch their first weight stages.
+  static constexpr int STAGES = BN <= 16 ? 4 : BN <= 32 ? 3 : BN <= 64 ? 4 : BN <= 128 ? 6 : 4;
   static constexpr int A_BYTES = kTileN * kTileK * 2;  // 16 KB
   static constexpr int B_BYTES = BN * kTileK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
