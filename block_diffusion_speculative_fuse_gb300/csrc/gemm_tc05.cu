@@ -585,7 +585,7 @@ static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int na = 0;
   if (pdl) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -598,6 +598,11 @@ static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
     attr[na].val.clusterDim.x = 1;
     attr[na].val.clusterDim.y = p.splits;
     attr[na].val.clusterDim.z = 1;
+    ++na;
+    // let several CTAs of a cluster share an SM, so clusters of 8 do not cap
+    // the number of resident CTAs
+    attr[na].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+    attr[na].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
     ++na;
   }
   cfg.attrs = attr;
