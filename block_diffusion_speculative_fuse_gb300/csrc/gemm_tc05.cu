@@ -457,6 +457,82 @@ __global__ void __launch_bounds__(128, 1)
       }
       do_epi = true;
     }
+  } else if (!p.cluster) {
+    // Split-K through global memory: every CTA stores its fp32 partial tile;
+    // the last CTA of the tile (atomic ticket, no waiting) sums the partials
+    // in split order and finishes the whole tile.
+    if (!aborted) {
+      float* part = p.partial + static_cast<size_t>(split) * p.M * p.N;
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 16, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = c * 16 + j;
+          if (r < rows) part[static_cast<size_t>(m0 + r) * p.N + n0 + f] = v[j];
+        }
+      }
+      __threadfence();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const int prev = aborted ? 0 : atomicAdd(&p.counters[mt * gridDim.x + tile], 1);
+      *last_flag = (!aborted && prev == p.splits - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (*last_flag) {
+      __threadfence();
+      const size_t sstride = static_cast<size_t>(p.M) * p.N / 4;  // float4 per split
+      const float4* pbase = reinterpret_cast<const float4*>(p.partial);
+      const int nchunk = rows * 32;
+      for (int c0 = tid; c0 < nchunk; c0 += 4 * 128) {
+        // up to 4 chunks per thread, splits in groups of 4: 16 loads in flight
+        const float4* src[4];
+        float4 acc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = c0 + i * 128;
+          src[i] = pbase + (static_cast<size_t>(m0 + (c < nchunk ? c / 32 : 0)) * p.N + n0) / 4 + c % 32;
+          acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        int sp = 0;
+        for (; sp + 4 <= p.splits; sp += 4) {
+          float4 v[4][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              v[i][j] = (c0 + i * 128 < nchunk) ? __ldcg(src[i] + (sp + j) * sstride)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              acc[i].x += v[i][j].x; acc[i].y += v[i][j].y;
+              acc[i].z += v[i][j].z; acc[i].w += v[i][j].w;
+            }
+        }
+        for (; sp < p.splits; ++sp) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (c0 + i * 128 < nchunk) {
+              const float4 v = __ldcg(src[i] + sp * sstride);
+              acc[i].x += v.x; acc[i].y += v.y; acc[i].z += v.z; acc[i].w += v.w;
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = c0 + i * 128;
+          if (c < nchunk)
+            *reinterpret_cast<float4*>(ts + (c / 32) * C::TS_LD + (c % 32) * 4) = acc[i];
+        }
+      }
+      if (tid == 0) p.counters[mt * gridDim.x + tile] = 0;
+      __syncthreads();
+      do_epi = true;
+    }
   } else {
     // 1) own partial tile -> own shared memory
     if (!aborted) {
@@ -547,7 +623,7 @@ __global__ void __launch_bounds__(128, 1)
       default: break;
     }
   }
-  if (p.splits > 1) cluster_sync();  // peers may still read this CTA's tile until here
+  if (p.splits > 1 && p.cluster) cluster_sync();  // peers may still read this CTA's tile until here
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
@@ -592,7 +668,7 @@ static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
-  if (p.splits > 1) {
+  if (p.splits > 1 && p.cluster) {
     // the split-K CTAs of one output tile form a cluster (reduced through DSMEM)
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = 1;
@@ -609,6 +685,42 @@ static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
   cfg.numAttrs = na;
   count_launch();
   return cudaLaunchKernelEx(&cfg, gemm_tc05_kernel<BN>, *w_map, *x_map, p);
+}
+
+template <int BN>
+static int max_clusters_bn(int cluster) {
+  using C = GemmCfg<BN>;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc05_kernel<BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, cluster, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = cluster;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc05_kernel<BN>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int gemm_max_active_clusters(int bn, int cluster) {
+  switch (bn) {
+    case 16: return max_clusters_bn<16>(cluster);
+    case 32: return max_clusters_bn<32>(cluster);
+    case 64: return max_clusters_bn<64>(cluster);
+    case 128: return max_clusters_bn<128>(cluster);
+    case 256: return max_clusters_bn<256>(cluster);
+    default: return 0;
+  }
 }
 
 cudaError_t gemm_launch(const CUtensorMap* w_map, const CUtensorMap* x_map, const GemmParams& p,

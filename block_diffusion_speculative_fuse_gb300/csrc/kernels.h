@@ -53,6 +53,7 @@ struct GemmParams {
   int w_tile_step;       // tensor-map rows advanced per output tile
   int w_half_gap;        // tensor-map row distance between the two 64-row halves
   int kb_total, kb_per_split, splits;
+  int cluster;           // splits > 1: 1 = reduce through a thread-block cluster (DSMEM), 0 = global
   float* partial;        // [splits][M][N] (splits > 1)
   int32_t* counters;     // [n_tiles * m_tiles], zero between launches
   int32_t* status;
@@ -88,6 +89,8 @@ struct GemmParams {
 // Picks the MMA N width for M rows and the split-K count.
 int gemm_bn_for(int M);
 int gemm_max_smem_bytes();
+// Clusters of `cluster` CTAs (BN variant) that can be resident at once.
+int gemm_max_active_clusters(int bn, int cluster);
 cudaError_t gemm_launch(const CUtensorMap* w_map, const CUtensorMap* x_map, const GemmParams& p,
                         int bn, cudaStream_t s, bool pdl);
 
