@@ -336,6 +336,9 @@ static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          attn_smem_bytes<D>());
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_kernel<D, NW>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     attr_device = dev;
   }
   const int G = p.hq / p.hkv;

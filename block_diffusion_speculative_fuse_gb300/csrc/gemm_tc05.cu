@@ -643,6 +643,19 @@ int gemm_max_smem_bytes() {
   return m;
 }
 
+// Dynamic shared memory size, and the largest shared-memory carveout so that
+// several CTAs (of this and of the next kernel) can be resident per SM.
+template <int BN>
+static cudaError_t set_gemm_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc05_kernel<BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       GemmCfg<BN>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm_tc05_kernel<BN>,
+                              cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
 template <int BN>
 static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
                              const GemmParams& p, cudaStream_t s, bool pdl) {
@@ -651,8 +664,7 @@ static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc05_kernel<BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaError_t e = set_gemm_attrs<BN>();
     if (e != cudaSuccess) return e;
     attr_device = dev;
   }
@@ -690,9 +702,7 @@ static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
 template <int BN>
 static int max_clusters_bn(int cluster) {
   using C = GemmCfg<BN>;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc05_kernel<BN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  if (e != cudaSuccess) return 0;
+  if (set_gemm_attrs<BN>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, cluster, 1);
   cfg.blockDim = dim3(128, 1, 1);
