@@ -75,7 +75,6 @@ struct dflash_model_s {
   int sms = 148;
   bool is_draft = false;
   CUtensorMap m_wqkv, m_wo, m_gu, m_down, m_lm, m_fc;
-  int max_clusters[5][9] = {};  // [log2(BN/16)][cluster size] resident clusters
   float2 rope[kMaxRopePairs];
   int qkv_rows = 0, q_dim = 0, kv_dim = 0;
 };
@@ -226,13 +225,12 @@ int run_gemm(const dflash_model_s* m, const CUtensorMap* wmap, const void* x, in
   const int mt = (p.M + bn - 1) / bn;
   p.cluster = 0;
   if (p.splits > 1) {
-    // reduce through DSMEM when every cluster of the grid is resident at once;
-    // otherwise through global memory (clusters would run in waves)
-    const int n_clusters = (p.N / kTileN) * mt;
-    p.cluster = (p.splits <= kMaxClusterSplits &&
-                 n_clusters <= m->max_clusters[bn_index(bn)][p.splits]) ? 1 : 0;
+    // split-K partials are reduced through distributed shared memory inside a
+    // cluster of the tile's splits (measured faster than a global-memory
+    // reduction even when the clusters run in more than one wave)
+    p.cluster = p.splits <= kMaxClusterSplits ? 1 : 0;
     if (!p.cluster) {
-      if (n_clusters > kMaxCounters) return DFLASH_ERR_CAPACITY;
+      if ((p.N / kTileN) * mt > kMaxCounters) return DFLASH_ERR_CAPACITY;
       p.partial = partial;
     }
   }
@@ -524,9 +522,6 @@ int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflas
     delete m;
     return rc;
   }
-  for (int bi = 0; bi < 5; ++bi)
-    for (int cs = 2; cs <= kMaxClusterSplits; ++cs)
-      m->max_clusters[bi][cs] = gemm_max_active_clusters(16 << bi, cs);
   // inv_freq_p = base^(-2p/d) as an unevaluated (hi, lo) float pair
   const int half = cfg->head_dim / 2;
   for (int p = 0; p < kMaxRopePairs; ++p) {
