@@ -10,7 +10,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/dflash.h"
+#include "dflash.h"
 
 namespace dflash {
 

@@ -9,7 +9,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/dflash.h"
+#include "dflash.h"
 #include "kernels.h"
 
 using namespace dflash;
