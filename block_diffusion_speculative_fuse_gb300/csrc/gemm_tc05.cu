@@ -26,11 +26,6 @@
 
 namespace dflash {
 
-// Weight k-blocks (beyond the shared-memory stages) a CTA prefetches into L2
-// before waiting for its predecessor kernel: weights do not depend on the
-// previous kernel, so they stream in while it drains.
-constexpr int kL2PrefetchKb = 8;
-
 template <int BN>
 struct GemmCfg {
   // BN <= 32 (decode-sized M): 3 CTAs fit per SM, so while a GEMM runs on two
@@ -388,14 +383,6 @@ __global__ void __launch_bounds__(128, 1)
       mbar_arrive_expect_tx(&full[it], C::STAGE_BYTES);
       tma_load_2d(a, &wmap, kx, wrow, &full[it], pol_w);
       tma_load_2d(a + C::A_BYTES / 2, &wmap, kx, wrow + p.w_half_gap, &full[it], pol_w);
-    }
-    {
-      const int pf_end = min(nkb, pre + kL2PrefetchKb);
-      for (int it = pre; it < pf_end; ++it) {
-        const int kx = (kb0 + it) * kTileK;
-        tma_prefetch_l2_2d(&wmap, kx, wrow);
-        tma_prefetch_l2_2d(&wmap, kx, wrow + p.w_half_gap);
-      }
     }
     griddep_wait();  // activations come from the previous kernel
     for (int it = 0; it < pre; ++it) {
