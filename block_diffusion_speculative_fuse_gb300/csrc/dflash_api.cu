@@ -217,7 +217,6 @@ GemmParams gemm_base(const dflash_model_s* m, int M, int N, int K, int bn, Ws& w
   return p;
 }
 
-int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn == 128 ? 3 : 4; }
 
 int run_gemm(const dflash_model_s* m, const CUtensorMap* wmap, const void* x, int ld_x,
              GemmParams& p, float* partial, cudaStream_t s) {
