@@ -88,17 +88,19 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
 
   griddep_launch_dependents();
   griddep_wait();
-  if (qt * R >= p.n) return;
+  if (qt * R >= p.n) return;  // uniform over the cluster (clusters span splits only)
   const int pos0 = p.pos0[req];
   const int S = p.split_keys;
-  int k_lo, k_hi;
+  // key range of this split; an empty range leaves (m, l, O) = (-inf, 0, 0)
+  int k_lo = 0, k_hi = 0;
   bool blk = false;
   if (p.causal) {
     const int last_row = min(p.n, (qt + 1) * R) - 1;
     const int kmax = pos0 + last_row + 1;
-    k_lo = split * S;
-    if (k_lo >= kmax) return;
-    k_hi = min(kmax, k_lo + S);
+    if (split * S < kmax) {
+      k_lo = split * S;
+      k_hi = min(kmax, k_lo + S);
+    }
   } else {
     const int nctx = (pos0 + S - 1) / S;
     if (split < nctx) {
@@ -108,10 +110,9 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
       blk = true;
       k_lo = 0;
       k_hi = p.n;
-    } else {
-      return;
     }
   }
+  if (!p.cluster && k_hi <= k_lo) return;
 
   // ---- query fragments (A operand, row-major 16 x D per warp)
   uint32_t qf[D / 16][4];
@@ -176,8 +177,8 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
 
   const int qpos0 = pos0 + row_lo + group;  // positions of this thread's two rows
   const int qpos1 = qpos0 + 8;
-  const int nch = (k_hi - k_lo + kChunk - 1) / kChunk;
-  load_chunk(0, k_lo);
+  const int nch = k_hi > k_lo ? (k_hi - k_lo + kChunk - 1) / kChunk : 0;
+  if (nch > 0) load_chunk(0, k_lo);
   for (int c = 0; c < nch; ++c) {
     if (c + 1 < nch) {
       load_chunk((c + 1) & 1, k_lo + (c + 1) * kChunk);
@@ -266,6 +267,75 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
     __syncthreads();
   }
 
+  if (p.cluster) {
+    // ---- combine across the cluster (the key splits of this query tile):
+    // stage unnormalised O and (m, l) in shared memory, then CTA q merges a
+    // share of the tile's query vectors from every peer, in split order.
+    constexpr int NV = 16 * NW;  // query vectors of the tile: (warp, row in 16)
+    float* Os = reinterpret_cast<float*>(sm);
+    float* MLs = Os + NV * D;
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int lv = warp * 16 + group + rr * 8;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        const int col = i * 8 + tq * 2;
+        *reinterpret_cast<float2*>(Os + lv * D + col) = make_float2(o[i][2 * rr], o[i][2 * rr + 1]);
+      }
+      if (tq == 0) {
+        MLs[lv * 2 + 0] = m_r[rr];
+        MLs[lv * 2 + 1] = l_r[rr];
+      }
+    }
+    const int SC = gridDim.x;
+    if (SC > 1) cluster_sync();
+    else __syncthreads();
+    const int q = SC > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int vpc = (NV + SC - 1) / SC;
+    const uint32_t os_addr = smem_u32(Os), ml_addr = smem_u32(MLs);
+    for (int lv = q * vpc + warp; lv < min(NV, (q + 1) * vpc); lv += NW) {
+      const int w = lv / 16, r = lv % 16;
+      const int row = qt * R + (w / G) * 16 + r;
+      const int hd = g * G + (w % G);
+      // lane s < SC fetches split s's (m, l)
+      float ms = -INFINITY, ls = 0.f;
+      if (lane < SC) {
+        const uint32_t a = (SC > 1 ? dsmem_map(ml_addr, lane) : ml_addr) + lv * 8;
+        float2 v;
+        asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+        ms = v.x;
+        ls = v.y;
+      }
+      const float mstar = warp_max(ms);
+      float acc[D / 32];
+#pragma unroll
+      for (int t = 0; t < D / 32; ++t) acc[t] = 0.f;
+      float lsum = 0.f;
+      for (int sp = 0; sp < SC; ++sp) {
+        const float msp = __shfl_sync(0xffffffffu, ms, sp);
+        const float lsp = __shfl_sync(0xffffffffu, ls, sp);
+        if (msp == -INFINITY) continue;
+        const float wgt = exp2f(msp - mstar);
+        lsum += lsp * wgt;
+        const uint32_t base = (SC > 1 ? dsmem_map(os_addr, sp) : os_addr) + (lv * D) * 4;
+#pragma unroll
+        for (int t = 0; t < D / 32; ++t) {
+          float v;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(base + (lane + 32 * t) * 4) : "memory");
+          acc[t] += v * wgt;
+        }
+      }
+      if (row < p.n) {
+        const float inv = 1.f / lsum;
+        uint16_t* out = p.out + ((static_cast<size_t>(req) * p.n + row) * p.hq + hd) * D;
+#pragma unroll
+        for (int t = 0; t < D / 32; ++t) out[lane + 32 * t] = f2bf(acc[t] * inv);
+      }
+    }
+    if (SC > 1) cluster_sync();  // peers may still read this CTA's partials until here
+    return;
+  }
+
   // ---- partial results: unnormalised O, running max (log2 domain) and sum
   const int rows_total = p.batch * p.n;
 #pragma unroll
@@ -346,16 +416,26 @@ static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  if (pdl) attrs[na++] = attr[0];
+  if (p.cluster && p.n_splits > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = p.n_splits;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_splits, (p.n + R - 1) / R, p.batch * p.hkv);
   cfg.blockDim = dim3(NW * 32, 1, 1);
   cfg.dynamicSmemBytes = attn_smem_bytes<D>();
   cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
   count_launch();
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_kernel<D, NW>, p);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || p.cluster) return e;
   cudaLaunchConfig_t c2 = {};
   const int vecs = p.batch * p.n * p.hq;
   c2.gridDim = dim3((vecs + 3) / 4, 1, 1);
@@ -365,6 +445,12 @@ static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
   c2.numAttrs = pdl ? 1 : 0;
   count_launch();
   return cudaLaunchKernelEx(&c2, attn_combine_kernel<D>, p);
+}
+
+bool attention_cluster_ok(int d, int hq, int hkv, int n_splits) {
+  // partials of a 4-warp tile (64 vectors x d fp32) are staged in the K/V
+  // buffers; 8-warp tiles and more than 8 splits use the global combine
+  return n_splits <= 8 && (hq / hkv) <= 4 && (d == 64 || d == 128);
 }
 
 cudaError_t attention_launch(const AttnParams& p, cudaStream_t s, bool pdl) {

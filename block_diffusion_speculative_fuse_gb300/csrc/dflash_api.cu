@@ -161,13 +161,15 @@ size_t partial_floats(const dflash_model_s* m, int rows_main, int rows_qkv) {
   return mx;
 }
 
+// Keys per attention split.  Drafter: at most 7 context splits + the block
+// split, so the splits of a query tile fit one cluster and combine through
+// DSMEM.  Target: a fixed 512 (split boundaries independent of the batch).
 int attn_split_keys(const dflash_model_s* m, int batch, int max_keys) {
+  (void)batch;
   if (!m->is_draft) return kTargetSplitKeys;
-  const long long work = static_cast<long long>(max_keys) * batch * m->cfg.n_kv_heads;
-  long long s = (work + 2LL * m->sms - 1) / (2LL * m->sms);
+  long long s = (static_cast<long long>(max_keys) + 6) / 7;
   s = ((s + 63) / 64) * 64;
-  s = std::max<long long>(128, std::min<long long>(2048, s));
-  return static_cast<int>(s);
+  return static_cast<int>(std::max<long long>(64, s));
 }
 int attn_n_splits(const dflash_model_s* m, int split_keys, int max_keys) {
   const int n = (max_keys + split_keys - 1) / split_keys;
@@ -362,6 +364,7 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       a.d = c.head_dim;
       a.split_keys = attn_split_keys(m, batch, max_keys);
       a.n_splits = attn_n_splits(m, a.split_keys, max_keys);
+      a.cluster = attention_cluster_ok(c.head_dim, c.n_q_heads, c.n_kv_heads, a.n_splits) ? 1 : 0;
       a.o_part = b.o_part;
       a.ml_part = b.ml_part;
       a.out = b.o;

@@ -107,6 +107,7 @@ struct AttnParams {
   int hq, hkv, d;
   int split_keys;        // keys per split, multiple of 64
   int n_splits;          // grid.x
+  int cluster;           // 1: the splits of a query tile form a cluster and combine through DSMEM
   float* o_part;         // [n_splits][batch*n][hq][d]
   float* ml_part;        // [n_splits][batch*n][hq][2]
   uint16_t* out;         // [batch*n][hq][d]
@@ -114,6 +115,7 @@ struct AttnParams {
 };
 cudaError_t attention_launch(const AttnParams& p, cudaStream_t s, bool pdl);
 size_t attention_part_floats(int n_splits, int rows, int hq, int d);
+bool attention_cluster_ok(int d, int hq, int hkv, int n_splits);
 
 // small kernels (small_kernels.cu)
 cudaError_t embed_block_launch(const int32_t* anchor, int batch, int block, const uint16_t* embed,
