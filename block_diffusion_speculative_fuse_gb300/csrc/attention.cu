@@ -357,6 +357,8 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
 }
 
 // One warp per (row, head): merge the splits that cover the row, in order.
+// Lane s holds split s's (m, l) (splits in groups of 32); the O partials of a
+// group are loaded together before they are accumulated in split order.
 template <int D>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   griddep_launch_dependents();
@@ -370,21 +372,48 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
   const int pos0 = p.pos0[req];
   const int S = p.split_keys;
   const int ns = p.causal ? (pos0 + i + 1 + S - 1) / S : (pos0 + S - 1) / S + 1;
+  const size_t vstride = static_cast<size_t>(rows_total) * p.hq;  // vectors per split
+  const size_t v0 = static_cast<size_t>(row) * p.hq + head;
   float mstar = -INFINITY;
-  for (int s = 0; s < ns; ++s)
-    mstar = fmaxf(mstar, p.ml_part[((static_cast<size_t>(s) * rows_total + row) * p.hq + head) * 2]);
+  for (int s0 = 0; s0 < ns; s0 += 32) {
+    const float ms = (s0 + lane < ns) ? p.ml_part[((s0 + lane) * vstride + v0) * 2] : -INFINITY;
+    mstar = fmaxf(mstar, warp_max(ms));
+  }
   float acc[D / 32];
 #pragma unroll
   for (int t = 0; t < D / 32; ++t) acc[t] = 0.f;
   float lsum = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const size_t vid = (static_cast<size_t>(s) * rows_total + row) * p.hq + head;
-    const float ms = p.ml_part[vid * 2];
-    if (ms == -INFINITY) continue;
-    const float w = exp2f(ms - mstar);
-    lsum += p.ml_part[vid * 2 + 1] * w;
+  for (int s0 = 0; s0 < ns; s0 += 32) {
+    const int sl = s0 + lane;
+    float ms = -INFINITY, ls = 0.f;
+    if (sl < ns) {
+      ms = p.ml_part[(sl * vstride + v0) * 2];
+      ls = p.ml_part[(sl * vstride + v0) * 2 + 1];
+    }
+    const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - mstar);
+    const int cnt = min(32, ns - s0);
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+      float v[8][D / 32];
+      float wj[8];
 #pragma unroll
-    for (int t = 0; t < D / 32; ++t) acc[t] += p.o_part[vid * D + lane + 32 * t] * w;
+      for (int j = 0; j < 8; ++j) {
+        wj[j] = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
+        const bool ok = j0 + j < cnt;
+#pragma unroll
+        for (int t = 0; t < D / 32; ++t)
+          v[j][t] = ok ? __ldcg(p.o_part + ((s0 + j0 + j) * vstride + v0) * D + lane + 32 * t) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j0 + j < cnt) {
+#pragma unroll
+          for (int t = 0; t < D / 32; ++t) acc[t] += v[j][t] * wj[j];
+        }
+      }
+    }
+    // l in split order (lane order)
+    float lw = ls * w;
+    for (int j = 0; j < cnt; ++j) lsum += __shfl_sync(0xffffffffu, lw, j);
   }
   const float inv = 1.f / lsum;
   uint16_t* out = p.out + (static_cast<size_t>(row) * p.hq + head) * D;
@@ -408,6 +437,8 @@ static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_kernel<D, NW>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_kernel<D, NW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_device = dev;
   }
@@ -448,9 +479,10 @@ static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
 }
 
 bool attention_cluster_ok(int d, int hq, int hkv, int n_splits) {
+  // clusters of up to 16 CTAs (non-portable size, supported on sm_103)
   // partials of a 4-warp tile (64 vectors x d fp32) are staged in the K/V
   // buffers; 8-warp tiles and more than 8 splits use the global combine
-  return n_splits <= 8 && (hq / hkv) <= 4 && (d == 64 || d == 128);
+  return n_splits <= kMaxAttnCluster && (hq / hkv) <= 4 && (d == 64 || d == 128);
 }
 
 cudaError_t attention_launch(const AttnParams& p, cudaStream_t s, bool pdl) {

@@ -161,13 +161,15 @@ size_t partial_floats(const dflash_model_s* m, int rows_main, int rows_qkv) {
   return mx;
 }
 
-// Keys per attention split.  Drafter: at most 7 context splits + the block
-// split, so the splits of a query tile fit one cluster and combine through
-// DSMEM.  Target: a fixed 512 (split boundaries independent of the batch).
+// Keys per attention split.  Drafter: at most kMaxAttnCluster-1 context
+// splits + the block split, so the splits of a query tile fit one cluster and
+// combine through DSMEM.  Target: a fixed 512 (split boundaries independent
+// of the batch).
 int attn_split_keys(const dflash_model_s* m, int batch, int max_keys) {
   (void)batch;
   if (!m->is_draft) return kTargetSplitKeys;
-  long long s = (static_cast<long long>(max_keys) + 6) / 7;
+  const int nc = kMaxAttnCluster - 1;
+  long long s = (static_cast<long long>(max_keys) + nc - 1) / nc;
   s = ((s + 63) / 64) * 64;
   return static_cast<int>(std::max<long long>(64, s));
 }

@@ -116,6 +116,7 @@ struct AttnParams {
 cudaError_t attention_launch(const AttnParams& p, cudaStream_t s, bool pdl);
 size_t attention_part_floats(int n_splits, int rows, int hq, int d);
 bool attention_cluster_ok(int d, int hq, int hkv, int n_splits);
+constexpr int kMaxAttnCluster = 16;
 
 // small kernels (small_kernels.cu)
 cudaError_t embed_block_launch(const int32_t* anchor, int batch, int block, const uint16_t* embed,
