@@ -156,7 +156,8 @@ size_t partial_floats(const dflash_model_s* m, int rows_main, int rows_qkv) {
     const int bn = gemm_bn_for(g.m_rows);
     const int mt = (g.m_rows + bn - 1) / bn;
     const int s = choose_splits(m, g.N / kTileN, mt, g.K / kTileK, bn);
-    if (s > 1) mx = std::max(mx, static_cast<size_t>(s) * g.m_rows * g.N);
+    // splits up to the cluster size reduce through DSMEM and need no buffer
+    if (s > kMaxClusterSplits) mx = std::max(mx, static_cast<size_t>(s) * g.m_rows * g.N);
   }
   return mx;
 }
