@@ -87,6 +87,8 @@ EXPORTS = {
                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                              ctypes.c_void_p]),
     "dflash_kernel_launches": (ctypes.c_uint64, []),
+    "dflash_ctx_fuse_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                               ctypes.c_void_p, ctypes.c_void_p]),
     "dflash_lm_head_argmax": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_size_t, ctypes.c_void_p]),
@@ -233,3 +235,10 @@ def dflash_lm_head_argmax(h, x, rows, argmax, logits, ws, stream=None):
 
 def dflash_kernel_launches() -> int:
     return int(load().dflash_kernel_launches())
+
+
+def dflash_ctx_fuse_noalloc(h, taps, T, ctx, stream=None):
+    """dflash_ctx_fuse without a workspace, for callers that cannot allocate
+    device memory; its scratch is a fixed array inside the library."""
+    return _check("dflash_ctx_fuse_noalloc", load().dflash_ctx_fuse_noalloc(
+        h, ptr(taps), T, ptr(ctx), stream_handle(stream)))

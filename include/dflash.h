@@ -168,6 +168,22 @@ int dflash_kv_append(dflash_model m, const void* ctx, const int32_t* row_req,
                      const int32_t* row_pos, int32_t T, const dflash_kv* kv, void* ws,
                      size_t ws_bytes, void* stream);
 
+/* dflash_ctx_fuse for callers that cannot allocate device memory (for
+ * example code running while another framework owns or has reserved the whole
+ * device memory pool, or that may not grow its footprint after start-up).  The
+ * pages describe no such call; it exists for deployment only.
+ * Same inputs and output as dflash_ctx_fuse, no workspace argument: the
+ * scratch is a fixed 4 MiB array inside the library, held by every GPU that
+ * loads the library until the process exits.  Needs 64 KiB + T*hidden*4 bytes
+ * of it (T <= 240 at hidden 4096); larger T returns DFLASH_ERR_CAPACITY.
+ * The first call on a device looks up the array's device address; make that
+ * first call before any stream capture.  All calls share the array (the
+ * header is cleared at the start of each call), so calls that may overlap on
+ * the GPU (different streams, or devices sharing a context) race.  Device-side
+ * status is not reported back. */
+int dflash_ctx_fuse_noalloc(dflash_model m, const void* taps, int32_t T, void* ctx,
+                            void* stream);
+
 /* One drafter pass for `batch` requests.  Request r's anchor token
  * anchor[r] sits at position L_r = anchor_pos[r]; block position i at L_r+i;
  * block rows attend to context positions [0, L_r) of the cache and to all B
