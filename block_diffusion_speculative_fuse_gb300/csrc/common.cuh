@@ -222,6 +222,17 @@ __device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
   return v;
 }
 
+// ---------------------------------------------------------------- barriers
+// Barrier over the whole CTA.
+struct CtaSync {
+  __device__ void operator()() const { __syncthreads(); }
+};
+// Barrier over the 128 threads of a named group (bar.sync id, 128).
+struct GroupSync {
+  int id;
+  __device__ void operator()() const { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+};
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

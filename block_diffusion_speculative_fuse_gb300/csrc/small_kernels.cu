@@ -82,10 +82,11 @@ __global__ void __launch_bounds__(kRowThreads)
     embed_block_kernel(const int32_t* anchor, int block, int n_blk, const uint16_t* embed,
                        const uint16_t* mask_embed, const uint16_t* g, int H, float* x,
                        uint16_t* a, int ld_a, float* ssq, const uint16_t* pending,
-                       int32_t* status, int vocab) {
+                       int32_t* status, int vocab, unsigned* zero_word) {
   griddep_launch_dependents();
   griddep_wait();
   const int r = blockIdx.x;
+  if (zero_word != nullptr && r == 0 && threadIdx.x == 0) *zero_word = 0u;
   if (r >= n_blk) {
     const uint16_t* src = pending + static_cast<size_t>(r - n_blk) * H;
     uint16_t* dst = a + static_cast<size_t>(r) * ld_a;
@@ -263,10 +264,11 @@ cudaError_t embed_block_launch(const int32_t* anchor, int batch, int block, cons
                                const uint16_t* mask_embed, const uint16_t* norm, int hidden,
                                float* x, uint16_t* a, int ld_a, float* ssq,
                                const uint16_t* pending, int T, cudaStream_t s, bool pdl,
-                               int32_t* status, int vocab) {
+                               int32_t* status, int vocab, unsigned* zero_word) {
   const int nb = batch * block;
   return launch(embed_block_kernel, dim3(nb + T), dim3(kRowThreads), 0, s, pdl, anchor, block, nb,
-                embed, mask_embed, norm, hidden, x, a, ld_a, ssq, pending, status, vocab);
+                embed, mask_embed, norm, hidden, x, a, ld_a, ssq, pending, status, vocab,
+                zero_word);
 }
 cudaError_t embed_tokens_launch(const int32_t* tokens, int rows, const uint16_t* embed,
                                 const uint16_t* norm, int hidden, float* x, uint16_t* a,
