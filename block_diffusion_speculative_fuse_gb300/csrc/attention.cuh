@@ -112,10 +112,11 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const int c = kk * 16 + tq * 2;
-      qf[kk][0] = v0 ? *reinterpret_cast<const uint32_t*>(q0 + c) : 0u;
-      qf[kk][1] = v1 ? *reinterpret_cast<const uint32_t*>(q1 + c) : 0u;
-      qf[kk][2] = v0 ? *reinterpret_cast<const uint32_t*>(q0 + c + 8) : 0u;
-      qf[kk][3] = v1 ? *reinterpret_cast<const uint32_t*>(q1 + c + 8) : 0u;
+      // L2-coherent loads: inside the persistent kernel q is rewritten every layer
+      qf[kk][0] = v0 ? __ldcg(reinterpret_cast<const unsigned int*>(q0 + c)) : 0u;
+      qf[kk][1] = v1 ? __ldcg(reinterpret_cast<const unsigned int*>(q1 + c)) : 0u;
+      qf[kk][2] = v0 ? __ldcg(reinterpret_cast<const unsigned int*>(q0 + c + 8)) : 0u;
+      qf[kk][3] = v1 ? __ldcg(reinterpret_cast<const unsigned int*>(q1 + c + 8)) : 0u;
     }
   }
 
@@ -299,7 +300,7 @@ __device__ __forceinline__ void attn_combine_vec(const AttnParams& p, int vec, i
   const size_t v0 = static_cast<size_t>(row) * p.hq + head;
   float mstar = -INFINITY;
   for (int s0 = 0; s0 < ns; s0 += 32) {
-    const float ms = (s0 + lane < ns) ? p.ml_part[((s0 + lane) * vstride + v0) * 2] : -INFINITY;
+    const float ms = (s0 + lane < ns) ? __ldcg(p.ml_part + ((s0 + lane) * vstride + v0) * 2) : -INFINITY;
     mstar = fmaxf(mstar, warp_max(ms));
   }
   float acc[D / 32];
@@ -310,8 +311,8 @@ __device__ __forceinline__ void attn_combine_vec(const AttnParams& p, int vec, i
     const int sl = s0 + lane;
     float ms = -INFINITY, ls = 0.f;
     if (sl < ns) {
-      ms = p.ml_part[(sl * vstride + v0) * 2];
-      ls = p.ml_part[(sl * vstride + v0) * 2 + 1];
+      ms = __ldcg(p.ml_part + (sl * vstride + v0) * 2);
+      ls = __ldcg(p.ml_part + (sl * vstride + v0) * 2 + 1);
     }
     const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - mstar);
     const int cnt = min(32, ns - s0);

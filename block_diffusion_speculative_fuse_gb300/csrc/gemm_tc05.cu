@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(128, 1)
     for (int r = warp; r < rows_v; r += 4) {
       const float* q = p.ssq_in + static_cast<size_t>(m0v + r) * p.ssq_in_tiles;
       float ss = 0.f;
-      for (int t = lane; t < p.ssq_in_tiles; t += 32) ss += q[t];
+      for (int t = lane; t < p.ssq_in_tiles; t += 32) ss += __ldcg(q + t);
       ss = warp_sum(ss);
       if (lane == 0)
         rinv[r] = (m0v + r < p.norm_rows) ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;

@@ -387,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float bv = -INFINITY;
           int bi = 0x7fffffff;
           for (int t = lane; t < n_tiles; t += 32) {
-            const float v = P.amax_val[static_cast<size_t>(row) * n_tiles + t];
-            const int j = P.amax_idx[static_cast<size_t>(row) * n_tiles + t];
+            const float v = __ldcg(P.amax_val + static_cast<size_t>(row) * n_tiles + t);
+            const int j = __ldcg(P.amax_idx + static_cast<size_t>(row) * n_tiles + t);
             if (v > bv || (v == bv && j < bi)) { bv = v; bi = j; }
           }
 #pragma unroll
@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int r = cw; r < g.M; r += 4) {
               const float* q = ssq_in + static_cast<size_t>(r) * (H / kTileN);
               float ss = 0.f;
-              for (int t = lane; t < H / kTileN; t += 32) ss += q[t];
+              for (int t = lane; t < H / kTileN; t += 32) ss += __ldcg(q + t);  // written by other CTAs
               ss = warp_sum(ss);
               if (lane == 0) rinv[r] = r < norm_rows ? rsqrtf(ss / static_cast<float>(H) + P.eps) : 1.f;
             }
