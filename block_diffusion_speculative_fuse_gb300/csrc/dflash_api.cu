@@ -525,7 +525,7 @@ int run_persistent(dflash_model_s* m, Ws& w, StackBufs& b, int batch, const int3
   DF_CUDA(embed_block_launch(anchor, batch, B, u16(m->w.embed), u16(m->w.mask_embed),
                              u16(m->w.in_norm), H, b.x, b.a, H, b.ssq_a, u16(pending_ctx), T, s,
                              true, w.status(), c.vocab, P.bar));
-  cudaError_t err = persistent_launch(P, m->sms, s);
+  cudaError_t err = persistent_launch(P, persistent_ctas(P, m->sms), s);
   if (err == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();
     m->persistent = false;
@@ -577,7 +577,8 @@ PersistParams persist_dims(const dflash_model_s* m) {
 }
 
 size_t persist_part_floats_for(const dflash_model_s* m) {
-  return persistent_part_floats(persist_dims(m), m->sms);
+  const PersistParams d = persist_dims(m);
+  return persistent_part_floats(d, persistent_ctas(d, m->sms));
 }
 
 int check_cfg(const dflash_config* c, bool draft) {

@@ -148,6 +148,7 @@ struct PersistParams {
   int32_t* status;
 };
 int persistent_smem_bytes();
+int persistent_ctas(const PersistParams& p, int sms);
 size_t persistent_part_floats(const PersistParams& p, int n_ctas);
 cudaError_t persistent_launch(const PersistParams& p, int n_ctas, cudaStream_t s);
 

@@ -499,6 +499,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int persistent_smem_bytes() { return kSmem; }
 
+// CTAs of the persistent launch: at most one per SM, and no more than the
+// smallest GEMM phase has (tile, k-block) iterations, so that every CTA owns at
+// least one iteration of every phase (the segment numbering relies on it).
+int persistent_ctas(const PersistParams& p, int sms) {
+  const long long tot[5] = {static_cast<long long>(p.qkv_rows / kTileN) * (p.H / kTileK),
+                            static_cast<long long>(p.H / kTileN) * (p.q_dim / kTileK),
+                            static_cast<long long>(2 * p.F / kTileN) * (p.H / kTileK),
+                            static_cast<long long>(p.H / kTileN) * (p.F / kTileK),
+                            static_cast<long long>(p.V / kTileN) * (p.H / kTileK)};
+  long long n = sms;
+  for (long long t : tot) n = n < t ? n : t;
+  return static_cast<int>(n);
+}
+
 // Largest tiles x segment-bound product over the GEMM phases (partial slots).
 size_t persistent_part_floats(const PersistParams& p, int nc) {
   struct Ph { long long n_tiles, kbt; };
