@@ -707,13 +707,18 @@ size_t dflash_workspace_bytes(dflash_model m, int32_t max_block_rows, int32_t ma
     StackBufs b;
     const int n = std::max(1, max_block_rows / max_batch);
     layout_stack(m, ws, b, max_batch, n, max_ctx_rows, max_keys);
-    // the attention partials are sized for the worst split count over batch sizes
+    // the attention partials are sized for the worst split count over batch
+    // sizes; calls with few enough rows also take the persistent kernel
     for (int bt = 1; bt <= max_batch; bt *= 2) {
-      Ws w2;
-      w2.dry = true;
-      StackBufs b2;
-      layout_stack(m, w2, b2, bt, std::max(1, max_block_rows / bt), max_ctx_rows, max_keys);
-      need = std::max(need, w2.off);
+      const int nb = std::max(1, max_block_rows / bt);
+      const int t_pers = std::max(0, std::min(max_ctx_rows, 32 - bt * nb));
+      for (int ctx : {max_ctx_rows, t_pers}) {
+        Ws w2;
+        w2.dry = true;
+        StackBufs b2;
+        layout_stack(m, w2, b2, bt, nb, ctx, max_keys);
+        need = std::max(need, w2.off);
+      }
     }
     need = std::max(need, ws.off);
   }
