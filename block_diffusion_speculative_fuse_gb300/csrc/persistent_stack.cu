@@ -197,12 +197,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pend_s[kStages], pend_k[kStages], pend_phi[kStages];
       const CUtensorMap* pend_x[kStages];
       int np = 0, it = 0;
+      int ready_phi = 0;  // phases <= ready_phi have their activations written
       bool dead = false;
+      // Poll the barrier counter and issue the activation loads that became
+      // valid.  Called only while blocked (full ring) or draining, so the
+      // steady-state stream issues no global loads.
       auto service = [&]() {
         if (np == 0) return;
         const unsigned c = ld_acquire(P.bar);
+        ready_phi = static_cast<int>(c / static_cast<unsigned>(nc));
         int k = 0;
-        while (k < np && c >= static_cast<unsigned>(pend_phi[k]) * nc) ++k;
+        while (k < np && pend_phi[k] <= ready_phi) ++k;
         if (k == 0) return;
         asm volatile("fence.proxy.async.global;" ::: "memory");
         for (int i = 0; i < k; ++i)
@@ -249,12 +254,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[s], kStageBytes);
           tma_load_2d(smem + s * kA, g.w, kx, wrow, &full[s], pol_w);
           tma_load_2d(smem + s * kA + kA / 2, g.w, kx, wrow + g.half_gap, &full[s], pol_w);
-          pend_s[np] = s;
-          pend_k[np] = kx;
-          pend_phi[np] = phi;
-          pend_x[np] = g.x;
-          ++np;
-          service();
+          if (np == 0 && phi <= ready_phi) {
+            tma_load_2d(smem + kStages * kA + s * kB, g.x, kx, 0, &full[s], pol_x);
+          } else {
+            pend_s[np] = s;
+            pend_k[np] = kx;
+            pend_phi[np] = phi;
+            pend_x[np] = g.x;
+            ++np;
+          }
         }
       }
       const uint64_t t0 = global_ns();
