@@ -251,3 +251,11 @@ def test_draft_step_verify_and_status_clean():
     assert np.array_equal(ref["out_tokens"], st.out_tokens.cpu().numpy())
     assert np.array_equal(ref["anchor_pos"], st.anchor_pos_out.cpu().numpy())
     assert st.step_counter.item() == 3
+
+
+def test_draft_block_parity_wide_batch():
+    """256 block rows (+ ragged context rows): the BN=256 GEMM path with
+    several activation-row tiles, ragged paged attention."""
+    wl = tiny_workload("wide", wid=796, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                       mlp=256, vocab=1024, block=16, batch=16, ctx_len_range=(16, 700))
+    check_draft_step(wl)
