@@ -40,9 +40,17 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 
 constexpr int kChunk = 64;
 
+// Physical page ids of one split's key range are staged in shared memory
+// (one parallel round trip) instead of being looked up per 16-byte piece.
+constexpr int kMaxSplitPages = 512;
+
+template <int D>
+__host__ __device__ constexpr int attn_kv_bytes() {
+  return 2 /*K,V*/ * 2 /*buffers*/ * kChunk * D * 2;
+}
 template <int D>
 __host__ __device__ constexpr int attn_smem_bytes() {
-  return 2 /*K,V*/ * 2 /*buffers*/ * kChunk * D * 2;
+  return attn_kv_bytes<D>() + kMaxSplitPages * 4;
 }
 
 // Byte offset of (key row, 16-byte column chunk) in a swizzled [64][D] tile.
@@ -121,6 +129,22 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
   }
 
   const size_t plane = static_cast<size_t>(p.hkv) * p.page_size * D;  // K->V plane distance
+  // stage this split's page ids (context keys only)
+  int* pages_s = reinterpret_cast<int*>(sm + attn_kv_bytes<D>());
+  const int page_lo = k_lo / p.page_size;
+  if (!blk && k_hi > k_lo) {
+    const int npg = (k_hi - 1) / p.page_size + 1 - page_lo;  // <= kMaxSplitPages (host caps S)
+    for (int i = tid; i < npg; i += NW * 32) {
+      const int pi = page_lo + i;
+      int pg = pi < p.max_pages ? p.page_table[static_cast<size_t>(req) * p.max_pages + pi] : -1;
+      if (pg < 0 || pg >= p.n_pages) {
+        raise_status(p.status, DFLASH_ERR_CAPACITY, 201);
+        pg = -1;
+      }
+      pages_s[i] = pg;
+    }
+    sync();
+  }
   auto load_chunk = [&](int buf, int kc) {
     constexpr int PIECES = kChunk * (D / 8);
     for (int pc = tid; pc < PIECES; pc += NW * 32) {
@@ -136,17 +160,13 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
           sv = p.vblk + o;
           bytes = 16;
         } else {
-          const int pi = key / p.page_size;
-          const int pg =
-              pi < p.max_pages ? p.page_table[static_cast<size_t>(req) * p.max_pages + pi] : -1;
-          if (pg >= 0 && pg < p.n_pages) {
+          const int pg = pages_s[key / p.page_size - page_lo];
+          if (pg >= 0) {
             const size_t o = (static_cast<size_t>(pg) * 2 * p.hkv + g) * p.page_size * D +
                              static_cast<size_t>(key % p.page_size) * D + ch * 8;
             sk = p.pool + o;
             sv = p.pool + o + plane;
             bytes = 16;
-          } else if (ch == 0) {
-            raise_status(p.status, DFLASH_ERR_CAPACITY, 201);
           }
         }
       }

@@ -175,6 +175,8 @@ int attn_split_keys(const dflash_model_s* m, int batch, int max_keys) {
   const int nc = kMaxAttnCluster - 1;
   long long s = (static_cast<long long>(max_keys) + nc - 1) / nc;
   s = ((s + 63) / 64) * 64;
+  // a split's page list must fit the staged page ids (kMaxSplitPages)
+  s = std::min<long long>(s, 8128);
   return static_cast<int>(std::max<long long>(64, s));
 }
 int attn_n_splits(const dflash_model_s* m, int split_keys, int max_keys) {

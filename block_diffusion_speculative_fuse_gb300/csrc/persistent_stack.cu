@@ -35,13 +35,13 @@ namespace dflash {
 
 namespace {
 
-constexpr int kStages = 8;
+constexpr int kStages = 7;
 constexpr int kBN = 32;                         // MMA N: activation rows, padded
 constexpr int kA = kTileN * kTileK * 2;         // 16 KB weight tile
 constexpr int kB = kBN * kTileK * 2;            // 4 KB activation tile
 constexpr int kStageBytes = kA + kB;
 constexpr int kRing = kStages * kStageBytes;    // 160 KB
-constexpr int kWork = 64 * 1024;                // attention K/V buffers or staged tile
+constexpr int kWork = 66 * 1024;                // attention K/V buffers + page ids, or staged tile
 constexpr int kCtl = 2048;                      // barriers, TMEM slot, row scales, routing
 constexpr int kSmem = kRing + kWork + kCtl + 1024;
 constexpr int kThreads = 192;
