@@ -207,15 +207,19 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
     float s[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+    // k-steps outer, the 8 key tiles inner: consecutive MMAs write different
+    // accumulators, so they issue back to back instead of waiting on each other
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int kk = 0; kk < D / 16; kk += 2) {
+      uint32_t bb[8][4];
 #pragma unroll
-      for (int kk = 0; kk < D / 16; kk += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + swz<D>(j * 8 + (lane & 7), kk * 2 + (lane >> 3)), b0, b1, b2, b3);
-        mma16816(s[j], qf[kk], b0, b1);
-        mma16816(s[j], qf[kk + 1], b2, b3);
-      }
+      for (int j = 0; j < 8; ++j)
+        ldsm_x4(kbase + swz<D>(j * 8 + (lane & 7), kk * 2 + (lane >> 3)), bb[j][0], bb[j][1],
+                bb[j][2], bb[j][3]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mma16816(s[j], qf[kk], bb[j][0], bb[j][1]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mma16816(s[j], qf[kk + 1], bb[j][2], bb[j][3]);
     }
     // mask + scale (log2 domain)
 #pragma unroll
