@@ -25,6 +25,8 @@
 
 namespace dflash {
 
+constexpr int kAttnBufs = 3;  // 96 KB of K/V chunks (d=128): 2 CTAs per SM
+
 template <int D, int NW>
 __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(128) uint8_t sm[];
@@ -37,7 +39,7 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
   griddep_launch_dependents();
   griddep_wait();
   AttnAcc<D> acc;
-  if (!attn_accumulate<D, NW>(p, split, qt, req, g, tid, sm, CtaSync{}, acc)) return;
+  if (!attn_accumulate<D, NW, kAttnBufs>(p, split, qt, req, g, tid, sm, CtaSync{}, acc)) return;
   const float (&o)[D / 8][4] = acc.o;
   const float* m_r = acc.m;
   const float* l_r = acc.l;
@@ -138,7 +140,7 @@ static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
   if (attr_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, NW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         attn_smem_bytes<D>());
+                                         attn_smem_bytes<D, kAttnBufs>());
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_kernel<D, NW>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
@@ -165,7 +167,7 @@ static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_splits, (p.n + R - 1) / R, p.batch * p.hkv);
   cfg.blockDim = dim3(NW * 32, 1, 1);
-  cfg.dynamicSmemBytes = attn_smem_bytes<D>();
+  cfg.dynamicSmemBytes = attn_smem_bytes<D, kAttnBufs>();
   cfg.stream = s;
   cfg.attrs = attrs;
   cfg.numAttrs = na;

@@ -44,13 +44,15 @@ constexpr int kChunk = 64;
 // (one parallel round trip) instead of being looked up per 16-byte piece.
 constexpr int kMaxSplitPages = 512;
 
-template <int D>
+// K/V chunk buffers of the cp.async pipeline (NBUF-1 chunks in flight ahead
+// of the one being computed).
+template <int D, int NBUF>
 __host__ __device__ constexpr int attn_kv_bytes() {
-  return 2 /*K,V*/ * 2 /*buffers*/ * kChunk * D * 2;
+  return 2 /*K,V*/ * NBUF * kChunk * D * 2;
 }
-template <int D>
+template <int D, int NBUF>
 __host__ __device__ constexpr int attn_smem_bytes() {
-  return attn_kv_bytes<D>() + kMaxSplitPages * 4;
+  return attn_kv_bytes<D, NBUF>() + kMaxSplitPages * 4;
 }
 
 // Byte offset of (key row, 16-byte column chunk) in a swizzled [64][D] tile.
@@ -70,12 +72,12 @@ struct AttnAcc {
 // over its key range, with NW warps (local thread index tid).  Leaves each
 // warp's unnormalised O and running (m, l) of its 16 query rows in acc.
 // Returns false when the query tile is past the request's rows.
-template <int D, int NW, typename Sync>
+template <int D, int NW, int NBUF, typename Sync>
 __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, int qt, int req,
                                                 int g, int tid, uint8_t* sm, Sync sync,
                                                 AttnAcc<D>& acc) {
   uint8_t* Kbuf = sm;
-  uint8_t* Vbuf = sm + 2 * kChunk * D * 2;
+  uint8_t* Vbuf = sm + NBUF * kChunk * D * 2;
 
   const int G = p.hq / p.hkv;
   const int R = 16 * NW / G;  // query rows per CTA
@@ -130,7 +132,7 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
 
   const size_t plane = static_cast<size_t>(p.hkv) * p.page_size * D;  // K->V plane distance
   // stage this split's page ids (context keys only)
-  int* pages_s = reinterpret_cast<int*>(sm + attn_kv_bytes<D>());
+  int* pages_s = reinterpret_cast<int*>(sm + attn_kv_bytes<D, NBUF>());
   const int page_lo = k_lo / p.page_size;
   if (!blk && k_hi > k_lo) {
     const int npg = (k_hi - 1) / p.page_size + 1 - page_lo;  // <= kMaxSplitPages (host caps S)
@@ -189,16 +191,23 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
   const int qpos0 = pos0 + row_lo + group;  // positions of this thread's two rows
   const int qpos1 = qpos0 + 8;
   const int nch = k_hi > k_lo ? (k_hi - k_lo + kChunk - 1) / kChunk : 0;
-  if (nch > 0) load_chunk(0, k_lo);
+  // prologue: the first NBUF-1 chunks (empty groups keep the count uniform)
+#pragma unroll
+  for (int c = 0; c < NBUF - 1; ++c) {
+    if (c < nch)
+      load_chunk(c, k_lo + c * kChunk);
+    else
+      cp_async_commit();
+  }
   for (int c = 0; c < nch; ++c) {
-    if (c + 1 < nch) {
-      load_chunk((c + 1) & 1, k_lo + (c + 1) * kChunk);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    // chunk c+NBUF-1 goes into the buffer freed at the end of iteration c-1
+    if (c + NBUF - 1 < nch)
+      load_chunk((c + NBUF - 1) % NBUF, k_lo + (c + NBUF - 1) * kChunk);
+    else
+      cp_async_commit();
+    cp_async_wait<NBUF - 1>();
     sync();
-    const int buf = c & 1;
+    const int buf = c % NBUF;
     const int kc = k_lo + c * kChunk;
     const uint32_t kbase = smem_u32(Kbuf) + buf * kChunk * D * 2;
     const uint32_t vbase = smem_u32(Vbuf) + buf * kChunk * D * 2;

@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           r /= n_qt;
           const int g = r % a.hkv, req = r / a.hkv;
           AttnAcc<D> acc;
-          if (attn_accumulate<D, 4>(ap, split, qt, req, g, ltid, work, gsync, acc))
+          if (attn_accumulate<D, 4, 2>(ap, split, qt, req, g, ltid, work, gsync, acc))
             attn_store_partial<D>(ap, split, req, acc, lane);
           gsync();  // the K/V buffers are reused by the next unit
         }
