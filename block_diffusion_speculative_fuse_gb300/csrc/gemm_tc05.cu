@@ -373,9 +373,12 @@ static cudaError_t set_gemm_attrs() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        GemmCfg<BN>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemm_tc05_kernel<BN>,
-                              cudaFuncAttributePreferredSharedMemoryCarveout,
-                              cudaSharedmemCarveoutMaxShared);
+  e = cudaFuncSetAttribute(gemm_tc05_kernel<BN>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  // split-K clusters of up to 16 CTAs (non-portable size, supported on sm_103)
+  return cudaFuncSetAttribute(gemm_tc05_kernel<BN>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                              1);
 }
 
 template <int BN>
