@@ -25,7 +25,7 @@
 
 namespace dflash {
 
-constexpr int kAttnBufs = 3;  // 96 KB of K/V chunks (d=128): 2 CTAs per SM
+constexpr int kAttnBufs = 2;  // double-buffered 64-key chunks (measured best)
 
 template <int D, int NW>
 __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ AttnParams p) {
