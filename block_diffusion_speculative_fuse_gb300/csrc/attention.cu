@@ -104,9 +104,14 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
       }
       if (row < p.n) {
         const float inv = 1.f / lsum;
-        uint16_t* out = p.out + ((static_cast<size_t>(req) * p.n + row) * p.hq + hd) * D;
+        const size_t ob = ((static_cast<size_t>(req) * p.n + row) * p.hq + hd) * D;
 #pragma unroll
-        for (int t = 0; t < D / 32; ++t) out[lane + 32 * t] = f2bf(acc[t] * inv);
+        for (int t = 0; t < D / 32; ++t) {
+          const float v = acc[t] * inv;
+          const uint16_t hi = f2bf(v);
+          p.out[ob + lane + 32 * t] = hi;
+          if (p.out_lo != nullptr) p.out_lo[ob + lane + 32 * t] = bf16_lo_part(v, hi);
+        }
       }
     }
     if (SC > 1) cluster_sync();  // peers may still read this CTA's partials until here

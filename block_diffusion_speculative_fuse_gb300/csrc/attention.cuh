@@ -373,9 +373,14 @@ __device__ __forceinline__ void attn_combine_vec(const AttnParams& p, int vec, i
     for (int j = 0; j < cnt; ++j) lsum += __shfl_sync(0xffffffffu, lw, j);
   }
   const float inv = 1.f / lsum;
-  uint16_t* out = p.out + (static_cast<size_t>(row) * p.hq + head) * D;
+  const size_t ob = (static_cast<size_t>(row) * p.hq + head) * D;
 #pragma unroll
-  for (int t = 0; t < D / 32; ++t) out[lane + 32 * t] = f2bf(acc[t] * inv);
+  for (int t = 0; t < D / 32; ++t) {
+    const float v = acc[t] * inv;
+    const uint16_t hi = f2bf(v);
+    p.out[ob + lane + 32 * t] = hi;
+    if (p.out_lo != nullptr) p.out_lo[ob + lane + 32 * t] = bf16_lo_part(v, hi);
+  }
 }
 
 }  // namespace dflash

@@ -42,6 +42,11 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
   __nv_bfloat16 h = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t*>(&h);
 }
+// v = hi + lo with hi = bf16(v), lo = bf16(v - hi) (the difference is exact
+// in fp32): a two-term bf16 expansion of v.
+__device__ __forceinline__ uint16_t bf16_lo_part(float v, uint16_t hi) {
+  return f2bf(v - bf2f(hi));
+}
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
   return static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
 }

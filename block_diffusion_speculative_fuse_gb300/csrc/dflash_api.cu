@@ -133,6 +133,11 @@ struct StackBufs {
   uint16_t* o;     // [rows][q_dim]
   uint16_t* a2;    // [rows][H]
   uint16_t* hmid;  // [rows][F]
+  // low bf16 halves of o, a2, hmid: the O-projection, gate/up and down GEMMs
+  // multiply the two-term expansion hi + lo of their activation operand
+  uint16_t* o_lo;
+  uint16_t* a2_lo;
+  uint16_t* hmid_lo;
   float* partial;
   float* amax_val;
   int32_t* amax_idx;
@@ -205,6 +210,9 @@ void layout_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int 
   b.o = ws.take<uint16_t>(static_cast<size_t>(rows) * m->q_dim);
   b.a2 = ws.take<uint16_t>(static_cast<size_t>(rows) * c.hidden);
   b.hmid = ws.take<uint16_t>(static_cast<size_t>(rows) * c.mlp);
+  b.o_lo = ws.take<uint16_t>(static_cast<size_t>(rows) * m->q_dim);
+  b.a2_lo = ws.take<uint16_t>(static_cast<size_t>(rows) * c.hidden);
+  b.hmid_lo = ws.take<uint16_t>(static_cast<size_t>(rows) * c.mlp);
   b.partial = ws.take<float>(partial_floats(m, rows, rows + ctx_rows));
   const int vt = c.vocab / kTileN;
   b.amax_val = ws.take<float>(static_cast<size_t>(rows) * vt);
@@ -235,8 +243,9 @@ GemmParams gemm_base(const dflash_model_s* m, int M, int N, int K, int bn, Ws& w
 }
 
 
+// x_lo (optional): low bf16 halves of the activation operand, same layout as x.
 int run_gemm(const dflash_model_s* m, const CUtensorMap* wmap, const void* x, int ld_x,
-             GemmParams& p, float* partial, cudaStream_t s) {
+             GemmParams& p, float* partial, cudaStream_t s, const void* x_lo = nullptr) {
   const int bn = gemm_bn_for(p.M);
   const int mt = (p.M + bn - 1) / bn;
   p.cluster = 0;
@@ -250,10 +259,11 @@ int run_gemm(const dflash_model_s* m, const CUtensorMap* wmap, const void* x, in
       p.partial = partial;
     }
   }
-  CUtensorMap xmap;
+  CUtensorMap xmap, xmap_lo;
   int rc = encode_map(&xmap, x, p.M, p.K, ld_x, bn);
+  if (!rc && x_lo != nullptr) rc = encode_map(&xmap_lo, x_lo, p.M, p.K, ld_x, bn);
   if (rc) return rc;
-  DF_CUDA(gemm_launch(wmap, &xmap, p, bn, s, true));
+  DF_CUDA(gemm_launch(wmap, &xmap, x_lo != nullptr ? &xmap_lo : nullptr, p, bn, s, true));
   return DFLASH_OK;
 }
 
@@ -383,6 +393,7 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       a.o_part = b.o_part;
       a.ml_part = b.ml_part;
       a.out = b.o;
+      a.out_lo = b.o_lo;
       a.status = ws.status();
       DF_CUDA(attention_launch(a, s, true));
     }
@@ -391,12 +402,13 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       GemmParams p = gemm_base(m, rows, H, m->q_dim, gemm_bn_for(rows), ws);
       p.w_row0 = l * H;
       set_resid_out(m, p, b.x, u16(m->w.post_norm) + static_cast<size_t>(l) * H, b.a2, b.ssq_a2);
+      p.xg_lo = b.a2_lo;
       if (m->is_draft && c.conv_width > 0 && m->w.conv != nullptr) {
         p.conv = u16(m->w.conv) + static_cast<size_t>(l) * H * c.conv_width;
         p.conv_width = c.conv_width;
         p.block = n;
       }
-      int rc = run_gemm(m, &m->m_wo, b.o, m->q_dim, p, b.partial, s);
+      int rc = run_gemm(m, &m->m_wo, b.o, m->q_dim, p, b.partial, s, b.o_lo);
       if (rc) return rc;
     }
     // gate/up + SwiGLU: each 128-row tile = 64 gate rows + the matching 64 up rows
@@ -407,9 +419,10 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       p.w_half_gap = c.mlp;
       p.mode = EPI_SWIGLU;
       p.out = b.hmid;
+      p.out_lo = b.hmid_lo;
       p.ld_out = c.mlp;
       set_norm_in(m, p, b.ssq_a2, rows);
-      int rc = run_gemm(m, &m->m_gu, b.a2, H, p, b.partial, s);
+      int rc = run_gemm(m, &m->m_gu, b.a2, H, p, b.partial, s, b.a2_lo);
       if (rc) return rc;
     }
     // down projection + residual -> next layer's in-norm input (or final norm)
@@ -424,7 +437,7 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
         p.raw_out = taps + static_cast<size_t>(tap_slot[l]) * H;
         p.ld_raw = n_taps * H;
       }
-      int rc = run_gemm(m, &m->m_down, b.hmid, c.mlp, p, b.partial, s);
+      int rc = run_gemm(m, &m->m_down, b.hmid, c.mlp, p, b.partial, s, b.hmid_lo);
       if (rc) return rc;
     }
   }

@@ -101,7 +101,12 @@ __device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int 
     const float x = ts[r * kTsLd + f];
     const size_t m = static_cast<size_t>(m0 + r);
     p.resid[m * p.ld_resid + n] = x;
-    if (p.xg_out != nullptr) p.xg_out[m * p.ld_xg + n] = f2bf(x * bf2f(p.gnext[n]));
+    if (p.xg_out != nullptr) {
+      const float xg = x * bf2f(p.gnext[n]);
+      const uint16_t hi = f2bf(xg);
+      p.xg_out[m * p.ld_xg + n] = hi;
+      if (p.xg_lo != nullptr) p.xg_lo[m * p.ld_xg + n] = bf16_lo_part(xg, hi);
+    }
     if (p.raw_out != nullptr) p.raw_out[m * p.ld_raw + n] = f2bf(x);
   }
   if (p.ssq_out != nullptr) {
@@ -128,7 +133,11 @@ __device__ void epi_swiglu(const GemmParams& p, const float* ts, int tile, int m
     const int r = idx / 64, j = idx % 64;
     const float g = ts[r * kTsLd + j];
     const float u = ts[r * kTsLd + 64 + j];
-    out[static_cast<size_t>(m0 + r) * p.ld_out + tile * 64 + j] = f2bf(silu_f(g) * u);
+    const float h = silu_f(g) * u;
+    const size_t o = static_cast<size_t>(m0 + r) * p.ld_out + tile * 64 + j;
+    const uint16_t hi = f2bf(h);
+    out[o] = hi;
+    if (p.out_lo != nullptr) p.out_lo[o] = bf16_lo_part(h, hi);
   }
 }
 

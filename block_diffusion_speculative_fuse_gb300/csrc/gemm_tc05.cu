@@ -27,15 +27,19 @@
 
 namespace dflash {
 
-template <int BN>
+template <int BN, bool SPLIT>
 struct GemmCfg {
   // BN <= 32 (decode-sized M): 3 CTAs fit per SM, so while a GEMM runs on two
   // slots the next kernel's CTAs (programmatic dependent launch) occupy the
-  // third and prefetch their first weight stages.
-  static constexpr int STAGES = BN <= 16 ? 4 : BN <= 32 ? 3 : BN <= 64 ? 4 : BN <= 128 ? 6 : 4;
+  // third and prefetch their first weight stages.  A split activation operand
+  // (hi + lo tiles) enlarges a stage, so those variants keep fewer stages.
+  static constexpr int STAGES =
+      SPLIT ? (BN <= 64 ? 3 : BN <= 128 ? 4 : 2)
+            : (BN <= 16 ? 4 : BN <= 32 ? 3 : BN <= 64 ? 4 : BN <= 128 ? 6 : 4);
   static constexpr int A_BYTES = kTileN * kTileK * 2;  // 16 KB
-  static constexpr int B_BYTES = BN * kTileK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int B_BYTES = BN * kTileK * 2;      // one activation tile
+  static constexpr int B_STAGE = SPLIT ? 2 * B_BYTES : B_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_STAGE;
   static constexpr int TS_LD = kTsLd;  // staged epilogue tile row stride (floats)
   static constexpr int TILE_BYTES = BN * TS_LD * 4;
   static constexpr int PIPE_BYTES = STAGES * STAGE_BYTES;
@@ -48,11 +52,13 @@ struct GemmCfg {
 };
 
 // ---------------------------------------------------------------- kernel
-template <int BN>
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(128, 1)
     gemm_tc05_kernel(const __grid_constant__ CUtensorMap wmap,
-                     const __grid_constant__ CUtensorMap xmap, const __grid_constant__ GemmParams p) {
-  using C = GemmCfg<BN>;
+                     const __grid_constant__ CUtensorMap xmap,
+                     const __grid_constant__ CUtensorMap xmap_lo,
+                     const __grid_constant__ GemmParams p) {
+  using C = GemmCfg<BN, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -82,6 +88,7 @@ __global__ void __launch_bounds__(128, 1)
     fence_barrier_init();
     tma_prefetch_desc(&wmap);
     tma_prefetch_desc(&xmap);
+    if (SPLIT) tma_prefetch_desc(&xmap_lo);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
@@ -106,8 +113,9 @@ __global__ void __launch_bounds__(128, 1)
     }
     griddep_wait();  // activations come from the previous kernel
     for (int it = 0; it < pre; ++it) {
-      uint8_t* b = smem + C::STAGES * C::A_BYTES + it * C::B_BYTES;
+      uint8_t* b = smem + C::STAGES * C::A_BYTES + it * C::B_STAGE;
       tma_load_2d(b, &xmap, (kb0 + it) * kTileK, m0, &full[it], pol_x);
+      if (SPLIT) tma_load_2d(b + C::B_BYTES, &xmap_lo, (kb0 + it) * kTileK, m0, &full[it], pol_x);
     }
     for (int it = pre; it < nkb; ++it) {
       const int s = it % C::STAGES;
@@ -118,12 +126,13 @@ __global__ void __launch_bounds__(128, 1)
         break;
       }
       uint8_t* a = smem + s * C::A_BYTES;
-      uint8_t* b = smem + C::STAGES * C::A_BYTES + s * C::B_BYTES;
+      uint8_t* b = smem + C::STAGES * C::A_BYTES + s * C::B_STAGE;
       const int kx = (kb0 + it) * kTileK;
       mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
       tma_load_2d(a, &wmap, kx, wrow, &full[s], pol_w);
       tma_load_2d(a + C::A_BYTES / 2, &wmap, kx, wrow + p.w_half_gap, &full[s], pol_w);
       tma_load_2d(b, &xmap, kx, m0, &full[s], pol_x);
+      if (SPLIT) tma_load_2d(b + C::B_BYTES, &xmap_lo, kx, m0, &full[s], pol_x);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer (single thread)
@@ -138,10 +147,14 @@ __global__ void __launch_bounds__(128, 1)
       }
       tc_fence_after();
       const uint64_t ad = umma_desc_sw128(smem_u32(smem + s * C::A_BYTES));
-      const uint64_t bd = umma_desc_sw128(smem_u32(smem + C::STAGES * C::A_BYTES + s * C::B_BYTES));
+      const uint32_t b_addr = smem_u32(smem + C::STAGES * C::A_BYTES + s * C::B_STAGE);
+      const uint64_t bd = umma_desc_sw128(b_addr);
 #pragma unroll
-      for (int k = 0; k < kTileK / 16; ++k)
+      for (int k = 0; k < kTileK / 16; ++k) {
         umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (it | k) != 0 ? 1u : 0u);
+        // W x_lo into the same accumulator: W (x_hi + x_lo)
+        if (SPLIT) umma_bf16(tmem, ad + 2 * k, umma_desc_sw128(b_addr + C::B_BYTES) + 2 * k, idesc, 1u);
+      }
       umma_commit(&empty[s]);
     }
     umma_commit(done);
@@ -356,40 +369,47 @@ int gemm_bn_for(int M) {
   return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
 }
 
-int gemm_max_smem_bytes() {
-  int m = GemmCfg<16>::SMEM_BYTES;
-  m = m > GemmCfg<32>::SMEM_BYTES ? m : GemmCfg<32>::SMEM_BYTES;
-  m = m > GemmCfg<64>::SMEM_BYTES ? m : GemmCfg<64>::SMEM_BYTES;
-  m = m > GemmCfg<128>::SMEM_BYTES ? m : GemmCfg<128>::SMEM_BYTES;
-  m = m > GemmCfg<256>::SMEM_BYTES ? m : GemmCfg<256>::SMEM_BYTES;
+template <bool SPLIT>
+static int max_smem_split() {
+  int m = GemmCfg<16, SPLIT>::SMEM_BYTES;
+  m = m > GemmCfg<32, SPLIT>::SMEM_BYTES ? m : GemmCfg<32, SPLIT>::SMEM_BYTES;
+  m = m > GemmCfg<64, SPLIT>::SMEM_BYTES ? m : GemmCfg<64, SPLIT>::SMEM_BYTES;
+  m = m > GemmCfg<128, SPLIT>::SMEM_BYTES ? m : GemmCfg<128, SPLIT>::SMEM_BYTES;
+  m = m > GemmCfg<256, SPLIT>::SMEM_BYTES ? m : GemmCfg<256, SPLIT>::SMEM_BYTES;
   return m;
+}
+int gemm_max_smem_bytes() {
+  const int a = max_smem_split<false>(), b = max_smem_split<true>();
+  return a > b ? a : b;
 }
 
 // Dynamic shared memory size, and the largest shared-memory carveout so that
 // several CTAs (of this and of the next kernel) can be resident per SM.
-template <int BN>
+template <int BN, bool SPLIT>
 static cudaError_t set_gemm_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc05_kernel<BN>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc05_kernel<BN, SPLIT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       GemmCfg<BN>::SMEM_BYTES);
+                                       GemmCfg<BN, SPLIT>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gemm_tc05_kernel<BN>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(gemm_tc05_kernel<BN, SPLIT>,
+                           cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   // split-K clusters of up to 16 CTAs (non-portable size, supported on sm_103)
-  return cudaFuncSetAttribute(gemm_tc05_kernel<BN>, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                              1);
+  return cudaFuncSetAttribute(gemm_tc05_kernel<BN, SPLIT>,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-template <int BN>
+template <int BN, bool SPLIT>
 static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
-                             const GemmParams& p, cudaStream_t s, bool pdl) {
-  using C = GemmCfg<BN>;
+                             const CUtensorMap* x_lo_map, const GemmParams& p, cudaStream_t s,
+                             bool pdl) {
+  using C = GemmCfg<BN, SPLIT>;
   static thread_local int attr_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_device != dev) {
-    cudaError_t e = set_gemm_attrs<BN>();
+    cudaError_t e = set_gemm_attrs<BN, SPLIT>();
     if (e != cudaSuccess) return e;
     attr_device = dev;
   }
@@ -421,13 +441,13 @@ static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
   cfg.attrs = attr;
   cfg.numAttrs = na;
   count_launch();
-  return cudaLaunchKernelEx(&cfg, gemm_tc05_kernel<BN>, *w_map, *x_map, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tc05_kernel<BN, SPLIT>, *w_map, *x_map, *x_lo_map, p);
 }
 
 template <int BN>
 static int max_clusters_bn(int cluster) {
-  using C = GemmCfg<BN>;
-  if (set_gemm_attrs<BN>() != cudaSuccess) return 0;
+  using C = GemmCfg<BN, false>;
+  if (set_gemm_attrs<BN, false>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, cluster, 1);
   cfg.blockDim = dim3(128, 1, 1);
@@ -440,7 +460,7 @@ static int max_clusters_bn(int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc05_kernel<BN>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc05_kernel<BN, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -458,14 +478,25 @@ int gemm_max_active_clusters(int bn, int cluster) {
   }
 }
 
-cudaError_t gemm_launch(const CUtensorMap* w_map, const CUtensorMap* x_map, const GemmParams& p,
-                        int bn, cudaStream_t s, bool pdl) {
+cudaError_t gemm_launch(const CUtensorMap* w_map, const CUtensorMap* x_map,
+                        const CUtensorMap* x_lo_map, const GemmParams& p, int bn, cudaStream_t s,
+                        bool pdl) {
+  if (x_lo_map != nullptr) {
+    switch (bn) {
+      case 16: return launch_bn<16, true>(w_map, x_map, x_lo_map, p, s, pdl);
+      case 32: return launch_bn<32, true>(w_map, x_map, x_lo_map, p, s, pdl);
+      case 64: return launch_bn<64, true>(w_map, x_map, x_lo_map, p, s, pdl);
+      case 128: return launch_bn<128, true>(w_map, x_map, x_lo_map, p, s, pdl);
+      case 256: return launch_bn<256, true>(w_map, x_map, x_lo_map, p, s, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (bn) {
-    case 16: return launch_bn<16>(w_map, x_map, p, s, pdl);
-    case 32: return launch_bn<32>(w_map, x_map, p, s, pdl);
-    case 64: return launch_bn<64>(w_map, x_map, p, s, pdl);
-    case 128: return launch_bn<128>(w_map, x_map, p, s, pdl);
-    case 256: return launch_bn<256>(w_map, x_map, p, s, pdl);
+    case 16: return launch_bn<16, false>(w_map, x_map, x_map, p, s, pdl);
+    case 32: return launch_bn<32, false>(w_map, x_map, x_map, p, s, pdl);
+    case 64: return launch_bn<64, false>(w_map, x_map, x_map, p, s, pdl);
+    case 128: return launch_bn<128, false>(w_map, x_map, x_map, p, s, pdl);
+    case 256: return launch_bn<256, false>(w_map, x_map, x_map, p, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

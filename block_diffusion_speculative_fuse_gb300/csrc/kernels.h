@@ -60,6 +60,12 @@ struct GemmParams {
   int mode;
   void* out;             // bf16/f32 store or SwiGLU output
   int ld_out;
+  // Optional low halves of the bf16 outputs that feed the next GEMM: the
+  // value v is stored as hi = bf16(v) plus lo = bf16(v - hi), and the consumer
+  // GEMM multiplies both (two MMAs into one accumulator), so the activation
+  // operand carries ~16 significant bits instead of 8.
+  uint16_t* out_lo;      // SwiGLU: [M][ld_out] next to out
+  uint16_t* xg_lo;       // EPI_RESID: [M][ld_xg] next to xg_out
   float* resid;
   int ld_resid;
   const uint16_t* conv;  // [N][conv_width] (this layer) or null
@@ -91,8 +97,11 @@ int gemm_bn_for(int M);
 int gemm_max_smem_bytes();
 // Clusters of `cluster` CTAs (BN variant) that can be resident at once.
 int gemm_max_active_clusters(int bn, int cluster);
-cudaError_t gemm_launch(const CUtensorMap* w_map, const CUtensorMap* x_map, const GemmParams& p,
-                        int bn, cudaStream_t s, bool pdl);
+// x_lo_map (nullable): the low halves of a split activation operand
+// (same shape as x_map); when given, every k-step issues a second MMA on it.
+cudaError_t gemm_launch(const CUtensorMap* w_map, const CUtensorMap* x_map,
+                        const CUtensorMap* x_lo_map, const GemmParams& p, int bn, cudaStream_t s,
+                        bool pdl);
 
 struct AttnParams {
   const uint16_t* q;     // [batch*n][hq][d]
@@ -111,6 +120,7 @@ struct AttnParams {
   float* o_part;         // [n_splits][batch*n][hq][d]
   float* ml_part;        // [n_splits][batch*n][hq][2]
   uint16_t* out;         // [batch*n][hq][d]
+  uint16_t* out_lo;      // optional low halves bf16(o - bf16(o)) for the O-projection GEMM
   int32_t* status;
 };
 cudaError_t attention_launch(const AttnParams& p, cudaStream_t s, bool pdl);
