@@ -1,0 +1,654 @@
+// Drafter attention on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// The block rows of a request attend, without a mask, to every context key
+// of the paged pool and to every key of the block itself (DFlash-2
+// mechanisms: the drafter is non-causal).  One CTA = (request, KV head, key
+// split); the key splits of a (request, KV head) form one thread-block
+// cluster (<= 16 CTAs) and merge their partial (O, m, l) through distributed
+// shared memory.
+//
+// Query rows: the G = hq/hkv query heads that share the KV head times the n
+// block rows, row index i*G + h (R = n*G rows).  Keys are streamed in chunks
+// of 64 (four 16-key pages) by TMA, one box per (page, K|V, 64-column half),
+// into a 4-deep ring of 128-byte-swizzled stages; pages past the split or
+// missing from the table are read from beyond the end of the tensor map,
+// which fills them with zeros.
+//
+// Per chunk c (warp 5 lane 0 issues, fp32 accumulators in TMEM):
+//   S[c%2] = Q K^T            M = 128 rows, N = 64 keys, K = head_dim
+//   O     += P[c%2] V         M = 128 rows, N = head_dim, K = 64 keys
+// Warps 0-3 own TMEM lanes 32w..32w+31.  Each thread reads its S row, masks
+// invalid keys and forms P = exp2(t - m) in the exp2 domain with a lazily
+// updated row maximum m: O and l are rescaled only when a chunk's maximum
+// exceeds m by more than 2^8 (so P <= 256), which keeps O in TMEM across
+// chunks.  P is stored in shared memory as the K-major A operand of the PV
+// MMA; V is the MN-major B operand.
+//
+// Two warp pairs (R <= 64): the query tile holds the R rows twice (MMA rows
+// 0-63 and 64-127), so every S tile carries the scores in both TMEM halves.
+// Warps 0-1 take the even chunks (lanes 0-63), warps 2-3 the odd chunks
+// (lanes 64-127); P[0] keeps rows 64-127 zero and P[1] rows 0-63, so the
+// even chunks accumulate into O lanes 0-63 and the odd ones into lanes
+// 64-127, two independent online-softmax states that are merged like key
+// splits.  With R > 64 all four warps take every chunk (one state).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dflash {
+
+namespace {
+
+constexpr int kChunkKeys = 64;
+constexpr int kChunkPages = 4;
+constexpr int kStages = 4;
+constexpr int kMaxPagesTc = 1024;  // pages per split (staged ids)
+constexpr float kRescaleLog2 = 8.f;
+constexpr int kThreads = 192;      // warps 0-3 softmax, 4 TMA, 5 MMA
+
+template <int D>
+struct TcCfg {
+  static constexpr int HALVES = D / 64;
+  static constexpr int Q_BYTES = 128 * D * 2;                   // [HALVES][128 rows][64]
+  static constexpr int P_BYTES = 128 * kChunkKeys * 2;          // [128 rows][64 keys]
+  static constexpr int KV_HALF = kChunkKeys * 64 * 2;           // [64 keys][64 cols] = 8 KB
+  static constexpr int K_BYTES = kChunkKeys * D * 2;            // [HALVES][64][64]
+  static constexpr int STAGE_BYTES = 2 * K_BYTES;               // K then V
+  static constexpr int BOXES = kChunkPages * 2 * HALVES;        // TMA boxes per chunk
+  static constexpr int Q_OFF = 0;
+  static constexpr int P_OFF = Q_OFF + Q_BYTES;
+  static constexpr int KV_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr int PG_OFF = KV_OFF + kStages * STAGE_BYTES;
+  static constexpr int PN_OFF = PG_OFF + kMaxPagesTc * 4;
+  static constexpr int BAR_OFF = PN_OFF + kMaxPagesTc * 4;
+  static constexpr int SMEM = BAR_OFF + 512 + 1024;             // barriers + alignment slack
+  // combine staging (after the key loop, in the K/V stage area): 128 row slots
+  // merge staging: at most 160 partial rows (rows per CTA x parts x splits
+  // <= (R + splits) x parts) of D + 4 floats plus (m, l)
+  static_assert(160 * ((D + 4) * 4 + 8) <= kStages * STAGE_BYTES, "merge staging must fit");
+  static_assert(BOXES <= 32, "one TMA box per producer lane");
+  static constexpr uint32_t TMEM_COLS = 256;                    // S0 | S1 | O
+  static constexpr uint32_t S_COL0 = 0, O_COL = 128;
+};
+
+__device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
+  return static_cast<uint32_t>(row * 128 + ((chunk16 ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc05_kernel(const __grid_constant__ CUtensorMap pool_map,
+                     const __grid_constant__ CUtensorMap kblk_map,
+                     const __grid_constant__ CUtensorMap vblk_map,
+                     const __grid_constant__ AttnTcParams p) {
+  using C = TcCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
+  uint64_t* kv_empty = kv_full + kStages;
+  uint64_t* s_full = kv_empty + kStages;  // [2]
+  uint64_t* s_free = s_full + 2;          // [2]
+  uint64_t* p_full = s_free + 2;          // [2]
+  uint64_t* pv_done = p_full + 2;         // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pv_done + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* pages_s = reinterpret_cast<int*>(sm + C::PG_OFF);   // pool page, -1 none, <= -2 block page
+  int* pages_n = reinterpret_cast<int*>(sm + C::PN_OFF);   // valid keys of each staged page
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int split = blockIdx.x;
+  const int req = blockIdx.y / p.hkv, g = blockIdx.y % p.hkv;
+  const int G = p.hq / p.hkv;
+  const int R = p.n * G;                        // real query rows (<= 128)
+  const bool dual = R <= 64;                    // two warp pairs, two softmax states
+  const int n_act = (R + 31) / 32;              // warps (per pair when dual) with real rows
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], n_act);
+      mbar_init(&p_full[b], n_act);
+      mbar_init(&pv_done[b], 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&pool_map);
+    tma_prefetch_desc(&kblk_map);
+    tma_prefetch_desc(&vblk_map);
+  }
+  if (warp == 5) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  // both P buffers start at zero: rows that no thread writes stay zero
+  for (int idx = tid; idx < 2 * C::P_BYTES / 16; idx += kThreads)
+    *reinterpret_cast<uint4*>(sm + C::P_OFF + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
+  griddep_launch_dependents();
+  griddep_wait();
+
+  // ---- one round of global loads, all issued before any is used: the
+  //      context length, this split's page ids (read before the length is
+  //      known) and the query rows
+  constexpr int QCH = D / 8;                                  // 16-byte pieces per row
+  constexpr int QMAX = (128 * QCH + kThreads - 1) / kThreads;
+  constexpr int PMAX = (kMaxPagesTc + kThreads - 1) / kThreads;
+  const int pg_lo = split * p.split_pages;
+  const int L = __ldcg(p.pos0 + req);
+  int pid[PMAX];
+#pragma unroll
+  for (int k = 0; k < PMAX; ++k) {
+    const int i = tid + k * kThreads, j = pg_lo + i;
+    pid[k] = (i < p.split_pages && j < p.max_pages)
+                 ? __ldcg(p.page_table + static_cast<size_t>(req) * p.max_pages + j)
+                 : -1;
+  }
+  const int qrows = dual ? 64 : 128;  // distinct tile rows (dual: rows 64-127 repeat 0-63)
+  uint4 qv[QMAX];
+#pragma unroll
+  for (int k = 0; k < QMAX; ++k) {
+    const int idx = tid + k * kThreads;
+    const int row = idx / QCH, c = idx % QCH;
+    qv[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (idx < qrows * QCH && row < R) {
+      const int i = row / G, h = row % G;
+      qv[k] = __ldcg(reinterpret_cast<const uint4*>(
+          p.q + ((static_cast<size_t>(req) * p.n + i) * p.hq + g * G + h) * D + c * 8));
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < QMAX; ++k) {
+    const int idx = tid + k * kThreads;
+    const int row = idx / QCH, c = idx % QCH;
+    if (idx < qrows * QCH) {
+      uint8_t* qb = sm + C::Q_OFF + (c / 8) * (128 * 128);
+      *reinterpret_cast<uint4*>(qb + swz128(row, c % 8)) = qv[k];
+      if (dual) *reinterpret_cast<uint4*>(qb + swz128(row + 64, c % 8)) = qv[k];
+    }
+  }
+  // ---- key space of this request: context pages [0, Pc), then block pages
+  const int Pc = (L + 15) / 16;
+  const int Pb = (p.n + 15) / 16;
+  const int pg_hi = min(Pc + Pb, pg_lo + p.split_pages);
+  const int npg = max(0, pg_hi - pg_lo);
+  const int nch = (npg + kChunkPages - 1) / kChunkPages;
+#pragma unroll
+  for (int k = 0; k < PMAX; ++k) {
+    const int i = tid + k * kThreads, j = pg_lo + i;
+    if (i >= nch * kChunkPages) continue;
+    int id = -1, cnt = 0;
+    if (i < npg) {
+      if (j < Pc) {
+        id = pid[k];
+        if (j >= p.max_pages || id < 0 || id >= p.n_pages) {
+          raise_status(p.status, DFLASH_ERR_CAPACITY, 301);
+          id = -1;
+        } else {
+          cnt = min(16, L - j * 16);
+        }
+      } else {
+        id = -2 - (j - Pc);
+        cnt = min(16, p.n - (j - Pc) * 16);
+      }
+    }
+    pages_s[i] = id;
+    pages_n[i] = cnt;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------ TMA producer (one box per lane)
+    const uint64_t pol = l2_policy_evict_first();
+    int issued = 0;
+    for (int c = 0; c < nch; ++c) {
+      const int st = c % kStages;
+      int ok = 1;
+      if (lane == 0) {
+        if (c >= kStages && !mbar_wait(&kv_empty[st], ((c / kStages) & 1) ^ 1, abort_flag)) {
+          *abort_flag = 1;
+          raise_status(p.status, DFLASH_ERR_TIMEOUT, 311);
+          ok = 0;
+        } else {
+          mbar_arrive_expect_tx(&kv_full[st], C::STAGE_BYTES);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane < C::BOXES) {
+        const int pp = lane / (2 * C::HALVES), kv = (lane / C::HALVES) % 2, hf = lane % C::HALVES;
+        const int id = pages_s[c * kChunkPages + pp];
+        const CUtensorMap* map = &pool_map;
+        int y;
+        if (id >= 0) {
+          y = p.pool_row0 + (id * 2 * p.hkv + g) * 16 + kv * p.hkv * 16;
+        } else if (id <= -2) {
+          map = kv ? &vblk_map : &kblk_map;
+          y = (req * p.hkv + g) * p.n + (-2 - id) * 16;
+        } else {
+          y = p.pool_rows;  // past the end: zero fill
+        }
+        uint8_t* dst = sm + C::KV_OFF + st * C::STAGE_BYTES + kv * C::K_BYTES + hf * C::KV_HALF +
+                       pp * 16 * 128;
+        tma_load_2d(dst, map, hf * 64, y, &kv_full[st], pol);
+      }
+      ++issued;
+    }
+    // copies still in flight after an abort land before the CTA exits
+    if (lane == 0)
+      for (int c = max(0, issued - kStages); c < issued; ++c)
+        mbar_wait(&kv_full[c % kStages], (c / kStages) & 1, nullptr);
+  } else if (warp == 5) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = umma_idesc_bf16(128, kChunkKeys);
+      constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D) | (1u << 16);  // B (V) MN-major
+      const uint32_t q_addr = smem_u32(sm + C::Q_OFF);
+      auto issue_s = [&](int c) -> bool {
+        const int st = c % kStages, b = c & 1;
+        if (!mbar_wait(&kv_full[st], (c / kStages) & 1, abort_flag)) return false;
+        if (c >= 2 && !mbar_wait(&s_free[b], ((c - 2) >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sm + C::KV_OFF + st * C::STAGE_BYTES);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k % 4) * 32;  // 16 K-elements within the 128-B row
+          const uint64_t ad = umma_desc_sw128(q_addr + (k / 4) * (128 * 128) + off);
+          const uint64_t bd = umma_desc_sw128(k_addr + (k / 4) * C::KV_HALF + off);
+          umma_bf16(tmem + C::S_COL0 + b * kChunkKeys, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[b]);
+        return true;
+      };
+      auto issue_pv = [&](int c) -> bool {
+        const int st = c % kStages, b = c & 1;
+        if (!mbar_wait(&p_full[b], (c >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t p_addr = smem_u32(sm + C::P_OFF + b * C::P_BYTES);
+        const uint32_t v_addr = smem_u32(sm + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES);
+#pragma unroll
+        for (int k = 0; k < kChunkKeys / 16; ++k) {
+          const uint64_t ad = umma_desc_sw128(p_addr + k * 32);
+          // keys 16k..16k+15 = rows of the V tile; d halves are C::KV_HALF apart
+          const uint64_t bd = umma_desc_sw128_mn(v_addr + k * 16 * 128, C::KV_HALF, 1024);
+          umma_bf16(tmem + C::O_COL, ad, bd, idesc_pv, (c > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(&pv_done[b]);
+        umma_commit(&kv_empty[st]);
+        return true;
+      };
+      bool ok = true;
+      if (nch > 0) ok = issue_s(0);
+      for (int c = 0; ok && c < nch; ++c) {
+        if (c + 1 < nch) ok = issue_s(c + 1);
+        if (ok) ok = issue_pv(c);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        raise_status(p.status, DFLASH_ERR_TIMEOUT, 312);
+      }
+    }
+  }
+
+  // ------------------------------------------------ softmax (warps 0-3)
+  const float sl2 = rsqrtf(static_cast<float>(D)) * 1.4426950408889634f;
+  const int pair = dual ? warp / 2 : 0;                      // meaningful for warps < 4
+  const int wip = dual ? warp % 2 : warp;                    // warp index within its pair
+  const int row_l = wip * 32 + lane;                         // query row of this thread
+  const bool active = warp < 4 && wip < n_act;
+  const int c_step = dual ? 2 : 1;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  float m_used = -INFINITY, l_sum = 0.f;
+  bool sm_ok = true;
+  if (active) {
+    for (int c = pair; c < nch; c += c_step) {
+      const int b = c & 1, st = c % kStages;
+      // every wait's outcome is made warp-uniform: the tcgen05.ld/st below are
+      // .sync.aligned and must be executed by all 32 lanes together
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (c >> 1) & 1, abort_flag))) { sm_ok = false; break; }
+      tc_fence_after();
+      uint32_t sr0[32], sr1[32];
+      tmem_ld32_nowait(lane_base + C::S_COL0 + b * kChunkKeys, sr0);
+      tmem_ld32_nowait(lane_base + C::S_COL0 + b * kChunkKeys + 32, sr1);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[b]);
+      int cntp[kChunkPages];
+      bool full = true, stale = false;
+#pragma unroll
+      for (int pp = 0; pp < kChunkPages; ++pp) {
+        cntp[pp] = pages_n[c * kChunkPages + pp];
+        full &= (cntp[pp] == 16);
+        stale |= (cntp[pp] > 0 && cntp[pp] < 16 && pages_s[c * kChunkPages + pp] >= 0);
+      }
+      float s[64];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        s[j] = __uint_as_float(sr0[j]);
+        s[32 + j] = __uint_as_float(sr1[j]);
+      }
+      if (!full) {
+        // invalid keys (stale or zero-filled rows) never contribute
+#pragma unroll
+        for (int j = 0; j < 64; ++j) s[j] = ((j % 16) < cntp[j / 16]) ? s[j] : -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(s[e], s[e + 8]);
+#pragma unroll
+      for (int j = 16; j < 64; j += 8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[j + e]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mc = mx * sl2;
+      // new reference maximum where the chunk's exceeds it by more than 2^8;
+      // O and l of such rows are rescaled (warp-collective: lanes that keep
+      // their maximum take alpha = 1)
+      const bool raise_m = mc > m_used + kRescaleLog2;
+      const bool rescale = raise_m && m_used != -INFINITY;
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag))) {
+          sm_ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float alpha = rescale ? ex2_approx(m_used - mc) : 1.f;
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32_nowait(lane_base + C::O_COL + q * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tmem_st32(lane_base + C::O_COL + q * 32, o);
+        }
+        tmem_wait_st();
+        l_sum *= alpha;
+      }
+      if (raise_m) m_used = mc;
+      // P = exp2(s*sl2 - m) in bf16 (masked keys: exp2(-inf) = 0)
+      const float neg = (m_used == -INFINITY) ? 0.f : -m_used;
+      uint32_t pk[32];
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float p0 = ex2_approx(fmaf(s[2 * j], sl2, neg));
+        const float p1 = ex2_approx(fmaf(s[2 * j + 1], sl2, neg));
+        pk[j] = pack_bf16x2(p0, p1);
+        ls4[j & 3] += p0 + p1;
+      }
+      l_sum += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+      // the P buffer b was last read by PV(c-2)
+      if (c >= 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag))) {
+        sm_ok = false;
+        break;
+      }
+      uint8_t* pbuf = sm + C::P_OFF + b * C::P_BYTES;
+      const int prow = warp * 32 + lane;  // MMA row = TMEM lane
+#pragma unroll
+      for (int c16 = 0; c16 < 8; ++c16)
+        *reinterpret_cast<uint4*>(pbuf + swz128(prow, c16)) =
+            make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+      if (stale) {
+        // rows past a context page's valid keys hold stale pool data: zero
+        // their V rows so that 0 * V stays 0
+        uint8_t* vst = sm + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
+        for (int idx = row_l; idx < kChunkKeys * C::HALVES * 8; idx += n_act * 32) {
+          const int key = idx / (C::HALVES * 8), rem = idx % (C::HALVES * 8);
+          const int hf = rem / 8, c16 = rem % 8;
+          if ((key % 16) >= cntp[key / 16])
+            *reinterpret_cast<uint4*>(vst + hf * C::KV_HALF + swz128(key, c16)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[b]);
+    }
+    if (!sm_ok) {
+      *abort_flag = 1;
+      if (lane == 0) raise_status(p.status, DFLASH_ERR_TIMEOUT, 313);
+    }
+    // the last PV of the CTA (it covers this pair's chunks too)
+    if (sm_ok && nch > 0 &&
+        !__all_sync(0xffffffffu, mbar_wait(&pv_done[(nch - 1) & 1], ((nch - 1) >> 1) & 1, abort_flag))) {
+      *abort_flag = 1;
+      if (lane == 0) raise_status(p.status, DFLASH_ERR_TIMEOUT, 314);
+    }
+  }
+
+  // ------------------------------------------------ partials -> owning CTAs
+  // CTA q of the cluster merges query rows [q*rpc, q*rpc + rpc).  After the
+  // first cluster barrier every CTA's K/V stages are free, and each thread
+  // stores its partial (O row, m, l) straight into the owner's stage area
+  // (remote stores, no round trip); after the second barrier the owner merges
+  // from its own shared memory.
+  __syncthreads();
+  const int SC = gridDim.x;
+  const int n_part = dual ? 2 : 1;
+  const int rpc = (R + SC - 1) / SC;
+  constexpr int OS_LD = D + 4;  // padded row stride (floats): conflict-free row stores
+  float* Rb = reinterpret_cast<float*>(sm + C::KV_OFF);     // [rpc][n_part][SC][OS_LD]
+  float* Rml = Rb + static_cast<size_t>(rpc) * n_part * SC * OS_LD;  // [rpc][n_part][SC][2]
+  cluster_sync();
+  tc_fence_after();
+  if (active) {  // warp-uniform: the tcgen05.ld below needs all 32 lanes
+    const bool have = __all_sync(0xffffffffu, nch > pair && !*abort_flag);
+    const bool mine = row_l < R;  // lanes past the real rows load but store nothing
+    const int own = mine ? row_l / rpc : 0, lr = row_l % rpc;
+    const int slot = (lr * n_part + pair) * SC + split;
+    const uint32_t dst = dsmem_map(smem_u32(Rb + static_cast<size_t>(slot) * OS_LD), own);
+#pragma unroll 1
+    for (int q = 0; q < D / 32; ++q) {
+      uint32_t o[32];
+      if (have) {
+        tmem_ld32_nowait(lane_base + C::O_COL + q * 32, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = 0u;
+      }
+      if (mine) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (q * 32 + j) * 4),
+                       "r"(o[j]), "r"(o[j + 1]), "r"(o[j + 2]), "r"(o[j + 3])
+                       : "memory");
+      }
+    }
+    if (mine) {
+      const float mv = have ? m_used : -INFINITY, lv = have ? l_sum : 0.f;
+      asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(
+                       dsmem_map(smem_u32(Rml + static_cast<size_t>(slot) * 2), own)),
+                   "f"(mv), "f"(lv)
+                   : "memory");
+    }
+  }
+  cluster_sync();
+
+  // ------------------------------------------------ merge (local shared memory)
+  {
+    const int q = static_cast<int>(cluster_ctarank());
+    constexpr int VEC = D / 32;  // floats per lane
+    for (int lr = warp; lr < rpc && q * rpc + lr < R; lr += kThreads / 32) {
+      const int r = q * rpc + lr;
+      // lane pi = part * SC + split holds that partial's (m, l)
+      float ms = -INFINITY, ls = 0.f;
+      if (lane < n_part * SC) {
+        const float2 v = *reinterpret_cast<const float2*>(Rml + (static_cast<size_t>(lr) * n_part * SC + lane) * 2);
+        ms = v.x;
+        ls = v.y;
+      }
+      const float mstar = warp_max(ms);
+      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - mstar);
+      const float lsum = warp_sum(w * ls);
+      float acc[VEC];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+      const float* rb = Rb + static_cast<size_t>(lr) * n_part * SC * OS_LD + lane * VEC;
+      for (int pi = 0; pi < n_part * SC; ++pi) {
+        const float wp = __shfl_sync(0xffffffffu, w, pi);
+        const float* src = rb + pi * OS_LD;
+        if constexpr (VEC == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          acc[0] = fmaf(v.x, wp, acc[0]);
+          acc[1] = fmaf(v.y, wp, acc[1]);
+          acc[2] = fmaf(v.z, wp, acc[2]);
+          acc[3] = fmaf(v.w, wp, acc[3]);
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          acc[0] = fmaf(v.x, wp, acc[0]);
+          acc[1] = fmaf(v.y, wp, acc[1]);
+        }
+      }
+      const float inv = 1.f / lsum;
+      const int i = r / G, h = r % G;
+      const size_t ob = ((static_cast<size_t>(req) * p.n + i) * p.hq + g * G + h) * D + lane * VEC;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const float v = acc[e] * inv;
+        const uint16_t hi = f2bf(v);
+        p.out[ob + e] = hi;
+        if (p.out_lo != nullptr) p.out_lo[ob + e] = bf16_lo_part(v, hi);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int D>
+cudaError_t launch_tc(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
+                      const CUtensorMap* vblk_map, const AttnTcParams& p, cudaStream_t s,
+                      bool pdl) {
+  static thread_local int attr_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc05_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_tc05_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    attr_device = dev;
+  }
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  if (pdl) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  attrs[na].id = cudaLaunchAttributeClusterDimension;
+  attrs[na].val.clusterDim.x = p.n_splits;
+  attrs[na].val.clusterDim.y = 1;
+  attrs[na].val.clusterDim.z = 1;
+  ++na;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_splits, p.batch * p.hkv, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = TcCfg<D>::SMEM;
+  cfg.stream = s;
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, attn_tc05_kernel<D>, *pool_map, *kblk_map, *vblk_map, p);
+}
+
+}  // namespace
+
+// Clusters of `cluster` CTAs (head_dim d) that can be resident at once.
+// Cached per device (value + 1; 0 = not yet queried).  The queries run at
+// model creation (attention_tc_prepare), outside any stream capture.
+constexpr int kMaxDevices = 64;
+static int g_active_clusters[kMaxDevices][2][kMaxAttnCluster + 1];
+
+static int max_active_clusters(int d, int cluster) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  int& slot = g_active_clusters[dev][d == 128 ? 1 : 0][cluster];
+  if (slot > 0) return slot - 1;
+  const void* fn = d == 128 ? reinterpret_cast<const void*>(attn_tc05_kernel<128>)
+                            : reinterpret_cast<const void*>(attn_tc05_kernel<64>);
+  const int smem = d == 128 ? TcCfg<128>::SMEM : TcCfg<64>::SMEM;
+  int n = 0;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  slot = n + 1;
+  return n;
+}
+
+void attention_tc_prepare(int d) {
+  for (int c = 1; c <= kMaxAttnCluster; ++c) max_active_clusters(d, c);
+}
+
+// Pages per key split.  Every (request, KV head) pair is one cluster of
+// splits; the estimate is the CTA-time of all pairs spread over the resident
+// CTA slots of that cluster size, but never less than one CTA's duration
+// (a fixed cost per CTA plus a cost per 64-key chunk).
+int attention_tc_split_pages(int d, int pairs, int total_pages) {
+  constexpr double kFixUs = 5.0, kChunkUs = 0.8;
+  double best = 1e30;
+  int best_sp = (total_pages + kMaxAttnCluster - 1) / kMaxAttnCluster;
+  for (int s = 1; s <= kMaxAttnCluster; ++s) {
+    const int sp = (total_pages + s - 1) / s;
+    if (sp > kMaxPagesTc) continue;
+    const int splits = (total_pages + sp - 1) / sp;
+    const int act = max_active_clusters(d, splits);
+    if (act <= 0) continue;
+    const double cta = kFixUs + ((sp + kChunkPages - 1) / kChunkPages) * kChunkUs;
+    const double fluid = static_cast<double>(pairs) * splits * cta / (static_cast<double>(act) * splits);
+    const double est = fluid > cta ? fluid : cta;
+    if (est < best * 0.999) {
+      best = est;
+      best_sp = sp;
+    }
+  }
+  return best_sp;
+}
+
+bool attention_tc_ok(int d, int hq, int hkv, int n, int page_size, int split_pages) {
+  return (d == 64 || d == 128) && page_size == 16 && hkv > 0 && hq % hkv == 0 &&
+         n * (hq / hkv) <= 128 && split_pages <= kMaxPagesTc;
+}
+
+cudaError_t attention_tc_launch(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
+                                const CUtensorMap* vblk_map, const AttnTcParams& p,
+                                cudaStream_t s, bool pdl) {
+  if (p.n_splits < 1 || p.n_splits > kMaxAttnCluster) return cudaErrorInvalidValue;
+  if (p.d == 128) return launch_tc<128>(pool_map, kblk_map, vblk_map, p, s, pdl);
+  if (p.d == 64) return launch_tc<64>(pool_map, kblk_map, vblk_map, p, s, pdl);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dflash

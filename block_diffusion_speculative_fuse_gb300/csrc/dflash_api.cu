@@ -76,6 +76,7 @@ struct dflash_model_s {
   int sms = 148;
   bool is_draft = false;
   bool persistent = false;  // use the persistent layer-stack kernel when the shape allows
+  bool attn_tc = true;      // drafter attention on tcgen05 (attention_tc05.cu) when the shape allows
   CUtensorMap m_wqkv, m_wo, m_gu, m_down, m_lm, m_fc;
   float2 rope[kMaxRopePairs];
   int qkv_rows = 0, q_dim = 0, kv_dim = 0;
@@ -338,6 +339,26 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
   const int rows = batch * n;
   const int H = c.hidden;
   const int max_keys = kv->max_pages * c.page_size;
+  // drafter attention on tcgen05: tensor maps over the pool and the block K/V
+  const int tc_pages = kv->max_pages + (n + 15) / 16;
+  const int tc_split_pages = attention_tc_split_pages(c.head_dim, batch * c.n_kv_heads, tc_pages);
+  const uint64_t pool_rows = static_cast<uint64_t>(c.n_layers) * kv->n_pages * 2 *
+                             c.n_kv_heads * 16;
+  const bool use_tc = m->is_draft && m->attn_tc &&
+                      attention_tc_ok(c.head_dim, c.n_q_heads, c.n_kv_heads, n, c.page_size,
+                                      tc_split_pages) &&
+                      pool_rows + 16 < (1ull << 31);
+  CUtensorMap pool_map, kblk_map, vblk_map;
+  if (use_tc) {
+    int rc = encode_map(&pool_map, kv->pool, pool_rows, c.head_dim, c.head_dim, 16);
+    if (!rc)
+      rc = encode_map(&kblk_map, b.kblk, static_cast<uint64_t>(rows) * c.n_kv_heads, c.head_dim,
+                      c.head_dim, 16);
+    if (!rc)
+      rc = encode_map(&vblk_map, b.vblk, static_cast<uint64_t>(rows) * c.n_kv_heads, c.head_dim,
+                      c.head_dim, 16);
+    if (rc) return rc;
+  }
   for (int l = 0; l < c.n_layers; ++l) {
     // QKV (+ context K/V rows in the same weight pass)
     {
@@ -369,7 +390,28 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       if (rc) return rc;
     }
     // attention
-    {
+    if (use_tc) {
+      AttnTcParams a;
+      std::memset(&a, 0, sizeof(a));
+      a.q = b.q;
+      a.batch = batch;
+      a.n = n;
+      a.pos0 = pos0;
+      a.page_table = kv->page_table;
+      a.max_pages = kv->max_pages;
+      a.n_pages = kv->n_pages;
+      a.hq = c.n_q_heads;
+      a.hkv = c.n_kv_heads;
+      a.d = c.head_dim;
+      a.pool_row0 = static_cast<int>(static_cast<uint64_t>(l) * kv->n_pages * 2 * c.n_kv_heads * 16);
+      a.pool_rows = static_cast<int>(pool_rows);
+      a.split_pages = tc_split_pages;
+      a.n_splits = (tc_pages + tc_split_pages - 1) / tc_split_pages;
+      a.out = b.o;
+      a.out_lo = b.o_lo;
+      a.status = ws.status();
+      DF_CUDA(attention_tc_launch(&pool_map, &kblk_map, &vblk_map, a, s, true));
+    } else {
       AttnParams a;
       std::memset(&a, 0, sizeof(a));
       a.q = b.q;
@@ -675,7 +717,12 @@ int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflas
     // the Qwen3-8B-shaped step it measured slower than the per-GEMM kernels.
     const char* e = std::getenv("DFLASH_PERSISTENT");
     m->persistent = (e != nullptr && e[0] == '1');
+    // DFLASH_ATTN_TC=0 keeps the drafter on the mma.sync attention kernel
+    const char* t = std::getenv("DFLASH_ATTN_TC");
+    m->attn_tc = !(t != nullptr && t[0] == '0');
   }
+  if (draft && m->attn_tc && (cfg->head_dim == 64 || cfg->head_dim == 128))
+    attention_tc_prepare(cfg->head_dim);
   m->q_dim = cfg->n_q_heads * cfg->head_dim;
   m->kv_dim = cfg->n_kv_heads * cfg->head_dim;
   m->qkv_rows = m->q_dim + 2 * m->kv_dim;

@@ -124,6 +124,35 @@ struct AttnParams {
   int32_t* status;
 };
 cudaError_t attention_launch(const AttnParams& p, cudaStream_t s, bool pdl);
+
+// Non-causal drafter attention on tcgen05 (attention_tc05.cu).  K/V come from
+// three 2-D bf16 tensor maps (box 16 rows x 64 columns, 128-byte swizzle):
+// the whole pool viewed as [n_layers*n_pages*2*hkv*16][d] rows, and the
+// block keys/values viewed as [batch*hkv*n][d].
+struct AttnTcParams {
+  const uint16_t* q;     // [batch*n][hq][d]
+  int batch, n;          // requests, block rows per request
+  const int32_t* pos0;   // [batch] context length (keys [0, pos0) in the pool)
+  const int32_t* page_table;
+  int max_pages, n_pages;
+  int hq, hkv, d;
+  int pool_row0;         // pool-map row of this layer's page 0
+  int pool_rows;         // rows of the pool map (a row index that reads as zeros)
+  int split_pages;       // 16-key pages per key split
+  int n_splits;          // key splits = cluster size (<= kMaxAttnCluster)
+  uint16_t* out;         // [batch*n][hq][d]
+  uint16_t* out_lo;      // optional low halves
+  int32_t* status;
+};
+cudaError_t attention_tc_launch(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
+                                const CUtensorMap* vblk_map, const AttnTcParams& p,
+                                cudaStream_t s, bool pdl);
+// Pages per key split for `pairs` (request, KV head) pairs over
+// `total_pages` 16-key pages (context pages + block pages).
+int attention_tc_split_pages(int d, int pairs, int total_pages);
+// Occupancy queries behind attention_tc_split_pages (call outside capture).
+void attention_tc_prepare(int d);
+bool attention_tc_ok(int d, int hq, int hkv, int n, int page_size, int split_pages);
 size_t attention_part_floats(int n_splits, int rows, int hq, int d);
 bool attention_cluster_ok(int d, int hq, int hkv, int n_splits);
 constexpr int kMaxAttnCluster = 16;

@@ -259,3 +259,30 @@ def test_draft_block_parity_wide_batch():
     wl = tiny_workload("wide", wid=796, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=128,
                        mlp=256, vocab=1024, block=16, batch=16, ctx_len_range=(16, 700))
     check_draft_step(wl)
+
+
+def test_draft_block_parity_mma_sync_attention(monkeypatch):
+    """The drafter on the mma.sync attention kernel (DFLASH_ATTN_TC=0, read at
+    model creation) still matches the oracle."""
+    monkeypatch.setenv("DFLASH_ATTN_TC", "0")
+    wl = tiny_workload("mmasync", wid=797, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                       mlp=256, vocab=1024, block=16, batch=3, ctx_len_range=(1, 900))
+    check_draft_step(wl)
+
+
+def test_draft_block_parity_wide_query_tile_fallback():
+    """block 32 x 8 query heads per KV head = 256 query rows per KV head: more
+    than one tcgen05 tile, so the drafter takes the mma.sync kernel."""
+    wl = tiny_workload("wideq", wid=798, hidden=512, n_q_heads=8, n_kv_heads=1, head_dim=64,
+                       mlp=256, vocab=1024, block=32, batch=2, ctx_len_range=(10, 400))
+    check_draft_step(wl)
+
+
+@pytest.mark.parametrize("d,wid", [(64, 799), (128, 800)])
+def test_draft_block_parity_single_softmax_state(d, wid):
+    """8 query heads per KV head x block 16 = 128 query rows per KV head, so
+    the tcgen05 attention runs one softmax state over all four warps instead
+    of two warp pairs."""
+    wl = tiny_workload("single", wid=wid, hidden=8 * d, n_q_heads=8, n_kv_heads=1, head_dim=d,
+                       mlp=256, vocab=1024, block=16, batch=2, ctx_len_range=(5, 700))
+    check_draft_step(wl)
