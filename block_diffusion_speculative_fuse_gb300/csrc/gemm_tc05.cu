@@ -44,8 +44,11 @@ struct GemmCfg {
   static constexpr int TILE_BYTES = BN * TS_LD * 4;
   static constexpr int PIPE_BYTES = STAGES * STAGE_BYTES;
   static constexpr int MAIN_BYTES = PIPE_BYTES > TILE_BYTES ? PIPE_BYTES : TILE_BYTES;
-  // epilogue scratch (row scales, QKV routing) sits after the staged tile
+  // epilogue scratch (row scales, QKV routing) sits after the staged tile;
+  // before the epilogue the same place receives the split-K partials pushed
+  // by the cluster peers ([splits][rows per CTA][128] fp32)
   static constexpr int SCRATCH_OFF = (TILE_BYTES + 255) / 256 * 256;
+  static constexpr int RECV_OFF = SCRATCH_OFF;
   static_assert(SCRATCH_OFF + 4 * BN * 4 <= MAIN_BYTES, "epilogue scratch must fit the pipeline region");
   static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + 1024;  // + barriers, alignment slack
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
@@ -179,6 +182,7 @@ __global__ void __launch_bounds__(128, 1)
   // split-K the S CTAs of the tile form one cluster and CTA q finishes rows
   // [q*rpc, q*rpc + rpc) (request-aligned when the block conv couples rows)
   int r_beg = 0, r_cnt = rows;
+  bool push = false;  // split-K partials pushed to their owners (no final barrier)
   if (p.splits == 1) {
     if (!aborted) {
 #pragma unroll 1
@@ -277,49 +281,83 @@ __global__ void __launch_bounds__(128, 1)
         for (int j = 0; j < 16; ++j) ts[(c * 16 + j) * C::TS_LD + f] = v[j];
       }
     }
-    cluster_sync();
-    // 2) reduce this CTA's rows over the cluster's partials (split order)
     const int S = p.splits;
     const int q = static_cast<int>(cluster_ctarank());
     int rpc = (rows + S - 1) / S;
     if (p.conv != nullptr && p.conv_width > 0) rpc = (rpc + p.block - 1) / p.block * p.block;
     r_beg = min(rows, q * rpc);
     r_cnt = min(rows, r_beg + rpc) - r_beg;
-    // Peers read only rows of their own range from this CTA's tile and this
-    // CTA overwrites only rows of its range, so the in-place write needs no
-    // extra barrier; the final cluster barrier keeps every tile alive until
-    // all peers are done reading.
-    const uint32_t ts_addr = smem_u32(ts);
-    const int nchunk = r_cnt * 32;  // float4 chunks of my rows
-    for (int c0 = tid; c0 < nchunk; c0 += 4 * 128) {
-      float4 red[4];
+    // Push when the partials of this CTA's rows fit its receive area (same
+    // decision in every CTA of the cluster: same tile rows and splits)
+    push = C::RECV_OFF + S * rpc * kTileN * 4 <= C::MAIN_BYTES;
+    if (push) {
+      __syncthreads();
+      cluster_sync();  // every peer has drained its pipeline: receive areas are free
+      // 2) each row of the tile -> slot [split] of the CTA that finishes it
+      const uint32_t recv_addr = smem_u32(smem + C::RECV_OFF);
+      for (int c = tid; c < rows * 32; c += 128) {
+        const int r = c / 32, c4 = c % 32;
+        const int own = r / rpc, lr = r % rpc;
+        const float4 v = *reinterpret_cast<const float4*>(ts + r * C::TS_LD + c4 * 4);
+        const uint32_t dst = dsmem_map(recv_addr + static_cast<uint32_t>(((split * rpc + lr) * 32 + c4) * 16),
+                                       static_cast<uint32_t>(own));
+        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(v.x), "f"(v.y),
+                     "f"(v.z), "f"(v.w)
+                     : "memory");
+      }
+      cluster_sync();  // all partials delivered
+      // 3) sum this CTA's rows over the splits in split order (local reads)
+      const float4* recv = reinterpret_cast<const float4*>(smem + C::RECV_OFF);
+      for (int c = tid; c < r_cnt * 32; c += 128) {
+        const int lr = c / 32, c4 = c % 32;
+        float4 acc = recv[lr * 32 + c4];
+        for (int sp = 1; sp < S; ++sp) {
+          const float4 v = recv[(sp * rpc + lr) * 32 + c4];
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        *reinterpret_cast<float4*>(ts + (r_beg + lr) * C::TS_LD + c4 * 4) = acc;
+      }
+      __syncthreads();
+      do_epi = !aborted && r_cnt > 0;
+    } else {
+      cluster_sync();
+      // 2) reduce this CTA's rows over the cluster's partials (split order)
+      // Peers read only rows of their own range from this CTA's tile and this
+      // CTA overwrites only rows of its range, so the in-place write needs no
+      // extra barrier; the final cluster barrier keeps every tile alive until
+      // all peers are done reading.
+      const uint32_t ts_addr = smem_u32(ts);
+      const int nchunk = r_cnt * 32;  // float4 chunks of my rows
+      for (int c0 = tid; c0 < nchunk; c0 += 4 * 128) {
+        float4 red[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) red[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < 4; ++i) red[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-      for (int sp = 0; sp < S; ++sp) {
-        const uint32_t peer = dsmem_map(ts_addr, static_cast<uint32_t>(sp));
-        float4 v[4];
+        for (int sp = 0; sp < S; ++sp) {
+          const uint32_t peer = dsmem_map(ts_addr, static_cast<uint32_t>(sp));
+          float4 v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = c0 + i * 128;
+            v[i] = c < nchunk
+                       ? dsmem_ld4(peer + static_cast<uint32_t>(((r_beg + c / 32) * C::TS_LD + (c % 32) * 4) * 4))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            red[i].x += v[i].x; red[i].y += v[i].y; red[i].z += v[i].z; red[i].w += v[i].w;
+          }
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int c = c0 + i * 128;
-          v[i] = c < nchunk
-                     ? dsmem_ld4(peer + static_cast<uint32_t>(((r_beg + c / 32) * C::TS_LD + (c % 32) * 4) * 4))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          red[i].x += v[i].x; red[i].y += v[i].y; red[i].z += v[i].z; red[i].w += v[i].w;
+          if (c < nchunk)
+            *reinterpret_cast<float4*>(ts + (r_beg + c / 32) * C::TS_LD + (c % 32) * 4) = red[i];
         }
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = c0 + i * 128;
-        if (c < nchunk)
-          *reinterpret_cast<float4*>(ts + (r_beg + c / 32) * C::TS_LD + (c % 32) * 4) = red[i];
-      }
+      __syncthreads();
+      do_epi = !aborted && r_cnt > 0;
     }
-    __syncthreads();
-    do_epi = !aborted && r_cnt > 0;
   }
   float* tsv = ts + r_beg * C::TS_LD;   // first row this CTA finishes
   const int m0v = m0 + r_beg;
@@ -358,7 +396,7 @@ __global__ void __launch_bounds__(128, 1)
       default: break;
     }
   }
-  if (p.splits > 1 && p.cluster) cluster_sync();  // peers may still read this CTA's tile until here
+  if (p.splits > 1 && p.cluster && !push) cluster_sync();  // peers may still read this CTA's tile until here
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
