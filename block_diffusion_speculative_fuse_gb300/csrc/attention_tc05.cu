@@ -613,9 +613,8 @@ void attention_tc_prepare(int d) {
 }
 
 // Pages per key split.  Every (request, KV head) pair is one cluster of
-// splits; the estimate is the CTA-time of all pairs spread over the resident
-// CTA slots of that cluster size, but never less than one CTA's duration
-// (a fixed cost per CTA plus a cost per 64-key chunk).
+// splits; the estimate is the number of waves of resident clusters times one
+// CTA's duration (a fixed cost per CTA plus a cost per 64-key chunk).
 int attention_tc_split_pages(int d, int pairs, int total_pages) {
   constexpr double kFixUs = 5.0, kChunkUs = 0.8;
   double best = 1e30;
@@ -627,8 +626,7 @@ int attention_tc_split_pages(int d, int pairs, int total_pages) {
     const int act = max_active_clusters(d, splits);
     if (act <= 0) continue;
     const double cta = kFixUs + ((sp + kChunkPages - 1) / kChunkPages) * kChunkUs;
-    const double fluid = static_cast<double>(pairs) * splits * cta / (static_cast<double>(act) * splits);
-    const double est = fluid > cta ? fluid : cta;
+    const double est = static_cast<double>((pairs + act - 1) / act) * cta;
     if (est < best * 0.999) {
       best = est;
       best_sp = sp;
