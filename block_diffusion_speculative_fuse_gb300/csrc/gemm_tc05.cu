@@ -363,16 +363,38 @@ __global__ void __launch_bounds__(128, 1)
   const int m0v = m0 + r_beg;
   const int rows_v = r_cnt;
   if (do_epi && p.ssq_in != nullptr) {
-    // one warp per row: the lanes read the row's per-tile sums together and
-    // combine them with a fixed butterfly (same order for any M)
+    // Sum of the row's per-tile sums in one fixed order for any M: lane t of
+    // a warp accumulates tiles t, t+32, ... and the 32 lane sums combine as
+    // the xor butterfly of warp_sum.  Up to 32 rows: one warp per row.  More
+    // rows: one thread per row computes the same sums with all of the row's
+    // loads in flight (a warp per row would wait one load round trip per row).
     float* rinv = reinterpret_cast<float*>(smem + C::SCRATCH_OFF);
-    for (int r = warp; r < rows_v; r += 4) {
-      const float* q = p.ssq_in + static_cast<size_t>(m0v + r) * p.ssq_in_tiles;
-      float ss = 0.f;
-      for (int t = lane; t < p.ssq_in_tiles; t += 32) ss += __ldcg(q + t);
-      ss = warp_sum(ss);
-      if (lane == 0)
-        rinv[r] = (m0v + r < p.norm_rows) ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
+    if (rows_v <= 32) {
+      for (int r = warp; r < rows_v; r += 4) {
+        const float* q = p.ssq_in + static_cast<size_t>(m0v + r) * p.ssq_in_tiles;
+        float ss = 0.f;
+        for (int t = lane; t < p.ssq_in_tiles; t += 32) ss += __ldcg(q + t);
+        ss = warp_sum(ss);
+        if (lane == 0)
+          rinv[r] = (m0v + r < p.norm_rows) ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
+      }
+    } else {
+      for (int r = tid; r < rows_v; r += 128) {
+        const float* q = p.ssq_in + static_cast<size_t>(m0v + r) * p.ssq_in_tiles;
+        float acc[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) acc[t] = 0.f;
+        for (int t0 = 0; t0 < p.ssq_in_tiles; t0 += 32) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (t0 + t < p.ssq_in_tiles) acc[t] += __ldcg(q + t0 + t);
+        }
+#pragma unroll
+        for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+          for (int t = 0; t < w; ++t) acc[t] += acc[t + w];
+        rinv[r] = (m0v + r < p.norm_rows) ? rsqrtf(acc[0] / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
+      }
     }
     __syncthreads();
     for (int idx = tid; idx < rows_v * kTileN; idx += 128) {
