@@ -146,7 +146,26 @@ __device__ void epi_argmax(const GemmParams& p, const float* ts, int tile, int m
                            int tid, Sync sync, int n_tiles) {
     const int warp = tid / 32, lane = tid % 32;
   const int n0 = tile * kTileN;
-  for (int r = warp; r < rows; r += 4) {
+  if (rows > 32) {
+    // one thread per row, features in increasing order: the first maximum
+    // is the lowest index, the same (value, index) as the warp reduction
+    for (int r = tid; r < rows; r += 128) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      const float4* row = reinterpret_cast<const float4*>(ts + r * kTsLd);
+#pragma unroll 8
+      for (int c4 = 0; c4 < kTileN / 4; ++c4) {
+        const float4 v = row[c4];
+        if (v.x > bv) { bv = v.x; bi = n0 + 4 * c4; }
+        if (v.y > bv) { bv = v.y; bi = n0 + 4 * c4 + 1; }
+        if (v.z > bv) { bv = v.z; bi = n0 + 4 * c4 + 2; }
+        if (v.w > bv) { bv = v.w; bi = n0 + 4 * c4 + 3; }
+      }
+      p.amax_val[static_cast<size_t>(m0 + r) * n_tiles + tile] = bv;
+      p.amax_idx[static_cast<size_t>(m0 + r) * n_tiles + tile] = bi;
+    }
+  }
+  for (int r = warp; r < (rows > 32 ? 0 : rows); r += 4) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
