@@ -92,8 +92,11 @@ def lm_head_bytes(d, rows):
 
 
 def source_sha():
-    p = os.path.join(ROOT, "block_diffusion_speculative_fuse_gb300", "csrc", "gemm_tc05.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    """Hash of the sources the LM-head GEMM kernel is compiled from."""
+    h = hashlib.sha256()
+    for f in ("gemm_tc05.cu", "epilogue.cuh", "common.cuh", "kernels.h"):
+        h.update(open(os.path.join(ROOT, "block_diffusion_speculative_fuse_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(config):
