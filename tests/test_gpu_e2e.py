@@ -98,3 +98,26 @@ def test_spec_equals_ar_other_block_sizes(block):
     ar = ar_generate(TargetRunner(tm, 2, 24 + 40 + 1, 24), prompt, 40)
     sd = SpecDecoder(tm, dm, wl.tap_layers, 2, 24 + 40)
     assert np.array_equal(sd.generate(prompt, 40), ar)
+
+
+def test_target_forward_rows_independent_of_batch():
+    """Batch invariance of the target path across the row-scale code paths:
+    3 requests x 16 rows in one call (48 rows per GEMM tile: one thread per
+    row for the deferred RMSNorm scale) give bit-identical logits to each
+    request alone (16 rows: one warp per row)."""
+    from block_diffusion_speculative_fuse_gb300.device import i32
+    from block_diffusion_speculative_fuse_gb300.generate import TargetRunner
+    wl = W.get_workload("tiny_e2e")
+    shared, tw, dw, tm, dm = models(wl, target_std=0.05)
+    V, n, b = wl.target.vocab, 16, 3
+    toks = W.uniform_tokens(b * n, V, wl.wid, W.TENSOR_IDS["prompt"], 7).reshape(b, n)
+    run3 = TargetRunner(tm, b, 64, n)
+    l3 = torch.zeros((b * n, V), dtype=torch.float32, device="cuda")
+    out3, _ = run3.forward(i32(toks), i32([0] * b), n, logits=l3)
+    for r in range(b):
+        run1 = TargetRunner(tm, 1, 64, n)
+        l1 = torch.zeros((n, V), dtype=torch.float32, device="cuda")
+        out1, _ = run1.forward(i32(toks[r:r + 1]), i32([0]), n, logits=l1)
+        torch.cuda.synchronize()
+        assert torch.equal(l1, l3[r * n:(r + 1) * n]), r
+        assert torch.equal(out1[0], out3[r])
