@@ -432,26 +432,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------ partials -> owning CTAs
-  // CTA q of the cluster merges query rows [q*rpc, q*rpc + rpc).  After the
-  // first cluster barrier every CTA's K/V stages are free, and each thread
-  // stores its partial (O row, m, l) straight into the owner's stage area
-  // (remote stores, no round trip); after the second barrier the owner merges
-  // from its own shared memory.
+  // With two warp pairs, the odd-chunk pair first hands its (O, m, l) to the
+  // even-chunk pair through local shared memory (the Q/P area, free once the
+  // last PV has completed), which merges the two states; one partial per row
+  // and split then remains.  CTA q of the cluster merges query rows
+  // [q*rpc, q*rpc + rpc): after the first cluster barrier every CTA's K/V
+  // stages are free, and each row's partial is stored straight into the
+  // owner's stage area (remote stores, no round trip); after the second
+  // barrier the owner merges from its own shared memory.
   __syncthreads();
+  tc_fence_after();
   const int SC = gridDim.x;
-  const int n_part = dual ? 2 : 1;
+  const int n_part = 1;
   const int rpc = (R + SC - 1) / SC;
   constexpr int OS_LD = D + 4;  // padded row stride (floats): conflict-free row stores
-  float* Rb = reinterpret_cast<float*>(sm + C::KV_OFF);     // [rpc][n_part][SC][OS_LD]
-  float* Rml = Rb + static_cast<size_t>(rpc) * n_part * SC * OS_LD;  // [rpc][n_part][SC][2]
-  cluster_sync();
-  tc_fence_after();
-  if (active) {  // warp-uniform: the tcgen05.ld below needs all 32 lanes
-    const bool have = __all_sync(0xffffffffu, nch > pair && !*abort_flag);
-    const bool mine = row_l < R;  // lanes past the real rows load but store nothing
-    const int own = mine ? row_l / rpc : 0, lr = row_l % rpc;
-    const int slot = (lr * n_part + pair) * SC + split;
-    const uint32_t dst = dsmem_map(smem_u32(Rb + static_cast<size_t>(slot) * OS_LD), own);
+  float* Xs = reinterpret_cast<float*>(sm + C::Q_OFF);       // [64][OS_LD] odd pair's O rows
+  float* Xml = Xs + 64 * OS_LD;                               // [64][2]
+  static_assert(64 * (D + 4) * 4 + 64 * 8 <= 2 * C::P_BYTES + C::Q_BYTES, "pair staging must fit Q/P");
+  const bool have = active && __all_sync(0xffffffffu, nch > pair && !*abort_flag);
+  if (dual && active && pair == 1) {  // warp-uniform
 #pragma unroll 1
     for (int q = 0; q < D / 32; ++q) {
       uint32_t o[32];
@@ -462,6 +461,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = 0u;
       }
+      float* dst = Xs + row_l * OS_LD + q * 32;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<uint4*>(dst + j) = make_uint4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+    }
+    Xml[row_l * 2 + 0] = have ? m_used : -INFINITY;
+    Xml[row_l * 2 + 1] = have ? l_sum : 0.f;
+  }
+  __syncthreads();
+  float* Rb = reinterpret_cast<float*>(sm + C::KV_OFF);     // [rpc][SC][OS_LD]
+  float* Rml = Rb + static_cast<size_t>(rpc) * n_part * SC * OS_LD;  // [rpc][SC][2]
+  cluster_sync();
+  tc_fence_after();
+  if (active && pair == 0) {  // warp-uniform: the tcgen05.ld below needs all 32 lanes
+    const bool mine = row_l < R;  // lanes past the real rows load but store nothing
+    const int own = mine ? row_l / rpc : 0, lr = row_l % rpc;
+    const int slot = lr * SC + split;
+    const uint32_t dst = dsmem_map(smem_u32(Rb + static_cast<size_t>(slot) * OS_LD), own);
+    // this pair's state and, with two pairs, the odd pair's
+    float m0 = have ? m_used : -INFINITY, l0 = have ? l_sum : 0.f;
+    float m1 = -INFINITY, l1 = 0.f;
+    if (dual) {
+      m1 = Xml[row_l * 2 + 0];
+      l1 = Xml[row_l * 2 + 1];
+    }
+    const float mx = fmaxf(m0, m1);
+    const float w0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - mx);
+    const float w1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - mx);
+#pragma unroll 1
+    for (int q = 0; q < D / 32; ++q) {
+      uint32_t o[32];
+      if (have) {
+        tmem_ld32_nowait(lane_base + C::O_COL + q * 32, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = 0u;
+      }
+      if (dual) {
+        const float* x = Xs + row_l * OS_LD + q * 32;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          o[j] = __float_as_uint(__uint_as_float(o[j]) * w0 + x[j] * w1);
+      }
       if (mine) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
@@ -471,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (mine) {
-      const float mv = have ? m_used : -INFINITY, lv = have ? l_sum : 0.f;
+      const float mv = dual ? mx : m0, lv = dual ? l0 * w0 + l1 * w1 : l0;
       asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(
                        dsmem_map(smem_u32(Rml + static_cast<size_t>(slot) * 2), own)),
                    "f"(mv), "f"(lv)
