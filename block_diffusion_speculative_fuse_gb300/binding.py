@@ -57,6 +57,8 @@ EXPORTS = {
                                            ctypes.POINTER(DflashWeights),
                                            ctypes.POINTER(ctypes.c_void_p)]),
     "dflash_model_destroy": (ctypes.c_int, [ctypes.c_void_p]),
+    "dflash_selftest_wait": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "dflash_workspace_bytes": (ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int32,
                                                  ctypes.c_int32, ctypes.c_int32,
                                                  ctypes.c_int32]),
@@ -181,6 +183,12 @@ def dflash_get_status(ws, stream=None):
                                                          ctypes.byref(site),
                                                          stream_handle(stream)))
     return st.value, site.value
+
+
+def dflash_selftest_wait(arrive, limit_ns, ws, waited_ns=None, stream=None):
+    return _check("dflash_selftest_wait", load().dflash_selftest_wait(
+        1 if arrive else 0, int(limit_ns), ptr(waited_ns), ptr(ws),
+        ws.numel() * ws.element_size(), stream_handle(stream)))
 
 
 def dflash_ctx_fuse(h, taps, T, ctx, ws, stream=None):

@@ -93,10 +93,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
       : "memory");
   return ok != 0;
 }
-// Bounded wait on phase `parity`; false after kWaitLimitNs or when *abort
+// Bounded wait on phase `parity`; false after limit_ns or when *abort
 // becomes non-zero (another role of the CTA gave up).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort_flag, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_ns();
@@ -104,8 +104,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(a, parity)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
+}
+// The kernels' wait: bounded by kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort_flag) {
+  return mbar_wait_for(bar, parity, abort_flag, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -1003,4 +1003,16 @@ int dflash_synth_target(const int32_t* draft, int32_t batch, int32_t B, const ui
   return DFLASH_OK;
 }
 
+int dflash_selftest_wait(int32_t arrive, int64_t limit_ns, int64_t* waited_ns, void* ws,
+                         size_t ws_bytes, void* stream) {
+  if (ws == nullptr || ws_bytes < kHeaderBytes || (reinterpret_cast<uintptr_t>(ws) & 255) ||
+      limit_ns < 1 || limit_ns > 1000000000LL ||
+      (reinterpret_cast<uintptr_t>(waited_ns) & 7))
+    return DFLASH_ERR_INVALID_ARG;
+  DF_CUDA(wait_selftest_launch(arrive != 0, static_cast<uint64_t>(limit_ns),
+                               static_cast<int*>(ws), waited_ns,
+                               static_cast<cudaStream_t>(stream)));
+  return DFLASH_OK;
+}
+
 }  // extern "C"

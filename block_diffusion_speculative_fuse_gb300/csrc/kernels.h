@@ -216,5 +216,7 @@ cudaError_t synth_target_launch(const int32_t* draft, int batch, int B, const ui
                                 int vocab, uint64_t seed, int64_t* step, int advance,
                                 int32_t* target, cudaStream_t s, bool pdl);
 cudaError_t copy_rows_f32_launch(const float* src, float* dst, size_t n, cudaStream_t s, bool pdl);
+cudaError_t wait_selftest_launch(int arrive, uint64_t limit_ns, int* status, int64_t* waited_ns,
+                                 cudaStream_t s);
 
 }  // namespace dflash

@@ -304,6 +304,31 @@ cudaError_t synth_target_launch(const int32_t* draft, int batch, int B, const ui
   return launch(synth_target_kernel, dim3(1), dim3(1024), 0, s, pdl, draft, batch, B, thr, vocab,
                 seed, step, advance, target);
 }
+// Self-test of the path every bounded wait takes when it runs out: thread 0
+// initialises an mbarrier in its own shared memory for one arrival, arrives
+// on it only when `arrive` is set, then waits for phase 0 for at most
+// limit_ns.  A wait that gives up records DFLASH_ERR_TIMEOUT (site 901) and
+// the kernel returns as usual.  No copy is ever issued on the barrier, so
+// nothing is left in flight when the kernel exits.
+__global__ void wait_selftest_kernel(int arrive, uint64_t limit_ns, int* status,
+                                     int64_t* waited_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (arrive) mbar_arrive(&bar);
+  const uint64_t t0 = global_ns();
+  const bool ok = mbar_wait_for(&bar, 0, nullptr, limit_ns);
+  const uint64_t t1 = global_ns();
+  if (!ok) raise_status(status, DFLASH_ERR_TIMEOUT, 901);
+  if (waited_ns != nullptr) *waited_ns = static_cast<int64_t>(t1 - t0);
+}
+
+cudaError_t wait_selftest_launch(int arrive, uint64_t limit_ns, int* status, int64_t* waited_ns,
+                                 cudaStream_t s) {
+  return launch(wait_selftest_kernel, dim3(1), dim3(32), 0, s, false, arrive, limit_ns, status,
+                waited_ns);
+}
 cudaError_t copy_rows_f32_launch(const float* src, float* dst, size_t n, cudaStream_t s, bool pdl) {
   const int blocks = static_cast<int>((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
   return launch(copy_f32_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, s, pdl, src, dst, n);

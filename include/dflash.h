@@ -250,6 +250,21 @@ int dflash_synth_target(const int32_t* draft, int32_t batch, int32_t B,
                         const uint64_t* threshold, int32_t vocab, uint64_t seed,
                         int64_t* step, int32_t advance, int32_t* target, void* stream);
 
+/* ------------------------------------------------------------ self-test */
+
+/* Exercises the device-side failure path without faulting anything (not a
+ * step of the method): one CTA waits, bounded by limit_ns, on an mbarrier in
+ * its own shared memory that gets its single arrival only when `arrive` is
+ * non-zero.  A wait that runs out records DFLASH_ERR_TIMEOUT with site 901 in
+ * the workspace status word and the kernel returns normally, which is what
+ * every bounded wait of the other kernels does (their limit is 1 s).
+ * limit_ns: 1 .. 10^9.  waited_ns: device int64 (may be NULL), receives the
+ * nanoseconds the wait took.  ws: an initialised workspace (only its status
+ * word is used).  Bad arguments return DFLASH_ERR_INVALID_ARG before any
+ * launch. */
+int dflash_selftest_wait(int32_t arrive, int64_t limit_ns, int64_t* waited_ns, void* ws,
+                         size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -104,3 +104,12 @@ def test_compute_calls_reject_null_handle(lib):
     assert lib.dflash_target_forward(None, d, d, 1, 1, ctypes.byref(kv), None, 0, None, d,
                                      None, d, 1 << 20, None) == -1
     assert lib.dflash_workspace_bytes(None, 16, 16, 1, 128) == 0
+
+
+def test_selftest_wait_rejects_bad_args_before_launch(lib):
+    ws = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails its checks
+    assert lib.dflash_selftest_wait(0, 1000, None, None, 1 << 16, None) == -1
+    assert lib.dflash_selftest_wait(0, 1000, None, ws, 1024, None) == -1
+    assert lib.dflash_selftest_wait(0, 0, None, ws, 1 << 16, None) == -1
+    assert lib.dflash_selftest_wait(0, 10**9 + 1, None, ws, 1 << 16, None) == -1
+    assert lib.dflash_selftest_wait(0, 1000, ctypes.c_void_p(4), ws, 1 << 16, None) == -1
