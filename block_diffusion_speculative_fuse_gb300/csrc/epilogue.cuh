@@ -202,7 +202,6 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
   const int d = e.head_dim;
   const int half = d / 2;
   const int per_tile = kTileN / d;
-  const int npair = half / 32;  // pairs per lane: 1 (d=64) or 2 (d=128)
   const int hq = e.n_q_heads, hkv = e.n_kv_heads;
   // Per-row routing, one thread per row, all lookups issued in parallel:
   // route[r] = (request, position, physical page or -1 for block rows / -2 skip)
@@ -239,66 +238,73 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
     r_pos[r] = pos;
     r_pg[r] = pg;
   }
-  float gq[4], gk[4];
+  // Each (row, head) item is handled by a group of 8 lanes, 4 items per warp
+  // at a time: lane `sub` of the group owns the rotate-half pairs
+  // [sub*P, sub*P + P), P = d/16, so its loads and stores are contiguous
+  // vectors and the head's sum of squares takes a 3-step butterfly.
+  const int grp = lane / 8, sub = lane % 8;
+  const int P = half / 8;  // 4 (d = 64) or 8 (d = 128)
+  const int c0 = sub * P;
+  float gq1[8], gq2[8], gk1[8], gk2[8];
+  float2 rf[8];
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int i = lane + 32 * t;
-    gq[t] = (e.q_norm != nullptr && i < d) ? bf2f(e.q_norm[i]) : 1.f;
-    gk[t] = (e.k_norm != nullptr && i < d) ? bf2f(e.k_norm[i]) : 1.f;
+  for (int j = 0; j < 8; ++j) {
+    const bool in = j < P;
+    gq1[j] = (in && e.q_norm != nullptr) ? bf2f(e.q_norm[c0 + j]) : 1.f;
+    gq2[j] = (in && e.q_norm != nullptr) ? bf2f(e.q_norm[half + c0 + j]) : 1.f;
+    gk1[j] = (in && e.k_norm != nullptr) ? bf2f(e.k_norm[c0 + j]) : 1.f;
+    gk2[j] = (in && e.k_norm != nullptr) ? bf2f(e.k_norm[half + c0 + j]) : 1.f;
+    rf[j] = in ? e.rope[c0 + j] : make_float2(0.f, 0.f);
   }
   sync();
-  for (int w = warp; w < rows * per_tile; w += 4) {
-    const int r = w / per_tile, hl = w % per_tile;
+  const int items = rows * per_tile;
+  // The loop bound depends on the warp only, so every lane reaches the
+  // shuffles; items past the end or skipped rows only drop their stores.
+  for (int w0 = warp * 4; w0 < items; w0 += 16) {
+    const int w = w0 + grp;
+    bool act = w < items;
+    const int r = act ? w / per_tile : 0, hl = act ? w % per_tile : 0;
     const int m = m0 + r;
     const int head = (e.f0 + tile * kTileN + hl * d) / d;
     const int kind = head < hq ? 0 : (head < hq + hkv ? 1 : 2);
     const int hidx = kind == 0 ? head : (kind == 1 ? head - hq : head - hq - hkv);
     const bool is_blk = m < e.n_blk;
     const int req = r_req[r], pos = r_pos[r], pg = r_pg[r];
-    if (!is_blk) {
-      if (pg == -2) continue;
-      if (kind == 0 && !e.keep_q_pool) continue;
-    }
-    const float* xs = ts + r * kTsLd + hl * d;
-    float x1[2], x2[2];
+    if (!is_blk && (pg == -2 || (kind == 0 && !e.keep_q_pool))) act = false;
+    const float* xs = ts + r * kTsLd + hl * d + c0;
+    float x1[8], x2[8];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      if (t < npair) {
-        x1[t] = xs[lane + 32 * t];
-        x2[t] = xs[lane + 32 * t + half];
+    for (int q = 0; q < 2; ++q) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (4 * q < P) {
+        a = *reinterpret_cast<const float4*>(xs + 4 * q);
+        b = *reinterpret_cast<const float4*>(xs + half + 4 * q);
       }
+      x1[4 * q] = a.x; x1[4 * q + 1] = a.y; x1[4 * q + 2] = a.z; x1[4 * q + 3] = a.w;
+      x2[4 * q] = b.x; x2[4 * q + 1] = b.y; x2[4 * q + 2] = b.z; x2[4 * q + 3] = b.w;
     }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += x1[j] * x1[j] + x2[j] * x2[j];  // zero past P
+    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     if (kind < 2) {
       const bool norm = kind == 0 ? (e.q_norm != nullptr) : (e.k_norm != nullptr);
-      if (norm) {
-        float ss = 0.f;
+      const float inv = norm ? rsqrtf(ss / static_cast<float>(d) + e.eps) : 1.f;
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (t < npair) ss += x1[t] * x1[t] + x2[t] * x2[t];
-        ss = warp_sum(ss);
-        const float inv = rsqrtf(ss / static_cast<float>(d) + e.eps);
-        // gain index lane+32t lives in slot t; its rotate-half partner in slot t + npair
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t < npair) {
-            const float ga = kind == 0 ? gq[t] : gk[t];
-            const float gb = kind == 0 ? gq[t + npair] : gk[t + npair];
-            x1[t] = x1[t] * inv * ga;
-            x2[t] = x2[t] * inv * gb;
-          }
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (t < npair) {
+      for (int j = 0; j < 8; ++j) {
+        if (j < P) {
+          const float a = x1[j] * inv * (kind == 0 ? gq1[j] : gk1[j]);
+          const float b = x2[j] * inv * (kind == 0 ? gq2[j] : gk2[j]);
           float sn, cs;
-          rope_sincos(pos, e.rope[lane + 32 * t], &sn, &cs);
-          const float a = x1[t], b = x2[t];
-          x1[t] = a * cs - b * sn;
-          x2[t] = b * cs + a * sn;
+          rope_sincos(pos, rf[j], &sn, &cs);
+          x1[j] = a * cs - b * sn;
+          x2[j] = b * cs + a * sn;
         }
       }
     }
+    if (!act) continue;
     uint16_t* dst;
     if (kind == 0) {
       dst = e.q + (static_cast<size_t>(m) * hq + hidx) * d;
@@ -309,12 +315,19 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
       dst = e.pool + ((((static_cast<size_t>(pg) * 2 + (kind - 1)) * hkv + hidx) * e.page_size) +
                       pos % e.page_size) * d;
     }
+    dst += c0;
+    uint32_t u1[4], u2[4];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      if (t < npair) {
-        dst[lane + 32 * t] = f2bf(x1[t]);
-        dst[lane + 32 * t + half] = f2bf(x2[t]);
-      }
+    for (int j = 0; j < 4; ++j) {
+      u1[j] = pack_bf2(x1[2 * j], x1[2 * j + 1]);
+      u2[j] = pack_bf2(x2[2 * j], x2[2 * j + 1]);
+    }
+    if (P == 8) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(u1[0], u1[1], u1[2], u1[3]);
+      *reinterpret_cast<uint4*>(dst + half) = make_uint4(u2[0], u2[1], u2[2], u2[3]);
+    } else {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(u1[0], u1[1]);
+      *reinterpret_cast<uint2*>(dst + half) = make_uint2(u2[0], u2[1]);
     }
   }
 }
