@@ -87,6 +87,23 @@ def step_flops(wl, ctx_before, new_rows):
     return dense + attn
 
 
+def acceptance_profile(hist, p):
+    """Per-position acceptance from hist[n] = number of (request, step)
+    samples that accepted n drafts (n = 0..B-1).  Block position i (1-based)
+    is accepted when n >= i.  The synthetic target agrees with the draft at
+    each position independently with its request's probability p_b, so the
+    expected rate at position i is the mean over requests of p_b**i."""
+    hist = np.asarray(hist, dtype=np.float64)
+    total = float(hist.sum())
+    n = np.arange(hist.size)
+    at_least = np.cumsum(hist[::-1])[::-1][1:] / total  # P(n >= i), i = 1..B-1
+    expected = np.mean(np.asarray(p, dtype=np.float64)[:, None] ** n[None, 1:], axis=0)
+    return {"samples": int(total),
+            "mean_accepted_drafts": float((hist * n).sum() / total),
+            "p_accept_at_position": [round(float(x), 4) for x in at_least],
+            "expected_p_accept_at_position": [round(float(x), 4) for x in expected]}
+
+
 def lm_head_bytes(d, rows):
     return 2 * d.vocab * d.hidden + 2 * rows * d.hidden + 4 * rows
 
@@ -331,14 +348,18 @@ def run_ours(args, rank, world, dist):
     if status[0] != 0:
         raise RuntimeError(f"device status {status} after the timed steps")
 
-    # acceptance: mean emitted tokens per step over fresh synthetic draws
+    # acceptance: mean emitted tokens per step over fresh synthetic draws, and
+    # the histogram of accepted draft counts (per-position acceptance)
     acc = torch.zeros(wl.batch, dtype=torch.int64, device="cuda")
+    hist = torch.zeros(d.block, dtype=torch.int64, device="cuda")
     with torch.cuda.stream(stream):
         for _ in range(args.accept_sample):
             one()
             acc += st.n_accept.long() + 1
+            hist += torch.bincount(st.n_accept.long(), minlength=d.block)[:d.block]
     stream.synchronize()
     emitted_per_step = float(acc.sum().item()) / args.accept_sample
+    accept_profile = acceptance_profile(hist.cpu().numpy(), W.agreement_probs(wl))
 
     # e2e through host buffers: H2D of the step's inputs, D2H of its outputs
     pin = lambda t: t.cpu().pin_memory()
@@ -408,6 +429,7 @@ def run_ours(args, rank, world, dist):
         "drafted_tokens_per_s": drafted,
         "accepted_tokens_per_s": accepted,
         "emitted_tokens_per_step": emitted_per_step,
+        "acceptance": accept_profile,
         "step_roofline": {"bound": "hbm", "bytes": sb, "flops": sf, "achieved": step_gbs,
                           "peak": hbm, "unit": "GB/s", "frac": step_gbs / hbm,
                           "peak_kind": pk_kind},
