@@ -18,5 +18,11 @@ token identity with autoregressive greedy decoding.  Parity unpinned: the
 numerical values of a full random-init draft step have no external
 reference (there is no trained model and no printed example); only the
 pinned pieces and invariants above vouch for them.
+
+``oracle.sampling`` holds the sampling-mode (temperature > 0) verify: the
+standard speculative-sampling acceptance rule applied to a block draft,
+pinned by brute force, its greedy limit, exact special cases and Monte Carlo
+checks of losslessness (tests/test_oracle_sampling.py).
 """
 from .dflash_oracle import *  # noqa: F401,F403
+from . import sampling  # noqa: F401,E402
