@@ -848,8 +848,9 @@ int dflash_ctx_fuse(dflash_model m, const void* taps, int32_t T, void* ctx, void
 int dflash_kv_append(dflash_model m, const void* ctx, const int32_t* row_req,
                      const int32_t* row_pos, int32_t T, const dflash_kv* kv, void* ws,
                      size_t ws_bytes, void* stream) {
-  if (m == nullptr || ctx == nullptr || row_req == nullptr || row_pos == nullptr || T < 1 ||
-      ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) || !aligned16(ctx))
+  if (m == nullptr || !m->is_draft || ctx == nullptr || row_req == nullptr ||
+      row_pos == nullptr || T < 1 || ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) ||
+      !aligned16(ctx))
     return DFLASH_ERR_INVALID_ARG;
   int rc = check_kv(m, kv);
   if (rc) return rc;

@@ -163,7 +163,8 @@ int dflash_ctx_fuse(dflash_model m, const void* taps, int32_t T, void* ctx, void
 
 /* For every layer l: K = RoPE(knorm(W_k^l c_t), pos_t), V = W_v^l c_t, stored
  * at logical position row_pos[t] of request row_req[t].  Rows with
- * row_pos[t] < 0 are skipped.  ctx: bf16 [T][hidden]. */
+ * row_pos[t] < 0 are skipped.  ctx: bf16 [T][hidden].  m must be a drafter
+ * (DFLASH_ERR_INVALID_ARG for a target model). */
 int dflash_kv_append(dflash_model m, const void* ctx, const int32_t* row_req,
                      const int32_t* row_pos, int32_t T, const dflash_kv* kv, void* ws,
                      size_t ws_bytes, void* stream);
@@ -215,7 +216,8 @@ int dflash_lm_head_argmax(dflash_model m, const void* x, int32_t rows, int32_t* 
  *   out_tokens [batch][B]: t_1..t_{n+1}, then -1;   n_accept [batch];
  *   tgt_len_out = tgt_len_in + n + 1;  ctx_pending = n + 1;
  *   anchor_out = t_{n+1};  anchor_pos_out = anchor_pos_in + n + 1.
- * In/out pairs may alias.  Pure integer work, bit-exact. */
+ * Any output may be NULL (not written); tgt_len_out and anchor_pos_out need
+ * their inputs.  In/out pairs may alias.  Pure integer work, bit-exact. */
 int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t batch, int32_t B,
                          int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
                          int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
