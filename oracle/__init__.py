@@ -23,6 +23,11 @@ pinned pieces and invariants above vouch for them.
 standard speculative-sampling acceptance rule applied to a block draft,
 pinned by brute force, its greedy limit, exact special cases and Monte Carlo
 checks of losslessness (tests/test_oracle_sampling.py).
+
+``oracle.fp8`` holds the E4M3 codec and per-(position, head) scaling for an
+fp8 context K/V cache and the study of its effect on the draft logits,
+pinned against the format's table and PyTorch's float8 cast
+(tests/test_oracle_fp8.py).
 """
 from .dflash_oracle import *  # noqa: F401,F403
-from . import sampling  # noqa: F401,E402
+from . import fp8, sampling  # noqa: F401,E402
