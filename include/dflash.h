@@ -164,7 +164,10 @@ int dflash_ctx_fuse(dflash_model m, const void* taps, int32_t T, void* ctx, void
 /* For every layer l: K = RoPE(knorm(W_k^l c_t), pos_t), V = W_v^l c_t, stored
  * at logical position row_pos[t] of request row_req[t].  Rows with
  * row_pos[t] < 0 are skipped.  ctx: bf16 [T][hidden].  m must be a drafter
- * (DFLASH_ERR_INVALID_ARG for a target model). */
+ * (DFLASH_ERR_INVALID_ARG for a target model).  row_req[t] must name a row
+ * of kv->page_table (0 <= row_req[t] < its row count): dflash_kv carries no
+ * row count, so the kernels check the page index and the page id they read
+ * but cannot check the request index. */
 int dflash_kv_append(dflash_model m, const void* ctx, const int32_t* row_req,
                      const int32_t* row_pos, int32_t T, const dflash_kv* kv, void* ws,
                      size_t ws_bytes, void* stream);
