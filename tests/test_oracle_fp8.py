@@ -5,7 +5,7 @@ PyTorch's own float8_e4m3fn cast (an independent implementation, compared
 where PyTorch does not turn large values into NaN), for round trips of every
 code and for ties and saturation.  The K/V scaling is checked against its
 error bound.  A slow test measures what fp8 storage of the context does to
-the Qwen3-8B-shaped drafter's logits.
+the draft logits of the Qwen3-8B-shaped and the DFlash-2 workloads.
 """
 import numpy as np
 import pytest
@@ -72,30 +72,41 @@ def test_kv_scaling_error_bound():
     assert np.all(y[5, 3] == 0.0) and scale[5, 3] == 1.0
 
 
-@pytest.mark.slow
-def test_fp8_context_study_qwen3_8b_shaped_step():
-    """The Qwen3-8B-shaped drafter at batch 1 (context 2048 + 16 rows): draft
-    logits with the context K/V in bf16 and in fp8.  Prints the measured
-    change; asserts only that the fp8 cache perturbs the logits (it is a
-    lossy format) and keeps every logit finite."""
-    wl = W.get_workload("qwen3_8b_b1")
+def fp8_study(name, req=0):
+    """Draft logits of one request of a workload with the context K/V in bf16
+    and in fp8; returns (max |dlogit|, rms, logit std, top-1 agreement,
+    rows)."""
+    wl = W.get_workload(name)
     d = wl.draft
     wid = wl.wid
     dws = O.LayerStack(d, W.draft_weights(d, wid), W.shared_weights(d, wid))
-    C = int(W.ctx_lengths(wl)[0])
-    T = int(W.new_row_counts(wl)[0])
-    c_rows = O.ctx_fuse(d, dws, O.bf16_to_f64(W.taps_bf16(T, d, wid)))
+    C = int(W.ctx_lengths(wl)[req])
+    new = W.new_row_counts(wl)
+    T, o = int(new[req]), int(new[:req].sum())
+    taps = W.taps_bf16(int(new.sum()), d, wid)[o:o + T]
+    c_rows = O.ctx_fuse(d, dws, O.bf16_to_f64(taps))
     ks, vs = [], []
     for l in range(d.n_layers):
         kn, vn = O.ctx_kv(d, dws, l, c_rows, np.arange(C, C + T))
-        ks.append(np.concatenate([O.bf16_to_f64(W.context_kv_bf16(d, wid, l, 0, C, "k")), kn]))
-        vs.append(np.concatenate([O.bf16_to_f64(W.context_kv_bf16(d, wid, l, 0, C, "v")), vn]))
-    anchor = int(W.uniform_tokens(1, d.vocab, wid, W.TENSOR_IDS["anchor"])[0])
+        ks.append(np.concatenate([O.bf16_to_f64(W.context_kv_bf16(d, wid, l, req, C, "k")), kn]))
+        vs.append(np.concatenate([O.bf16_to_f64(W.context_kv_bf16(d, wid, l, req, C, "v")), vn]))
+    anchor = int(W.uniform_tokens(wl.batch, d.vocab, wid, W.TENSOR_IDS["anchor"])[req])
     ref, q8 = F.kv_study(d, dws, anchor, C + T, ks, vs, O.draft_block)
+    assert np.all(np.isfinite(q8))
     diff = np.abs(q8 - ref)[1:]
     agree = float(np.mean(np.argmax(q8[1:], -1) == np.argmax(ref[1:], -1)))
-    print(f"\nfp8 context K/V, Qwen3-8B-shaped b1: max|dlogit| {diff.max():.4f}, "
-          f"rms {np.sqrt((diff ** 2).mean()):.5f}, logit std {ref[1:].std():.3f}, "
-          f"top-1 agreement {agree:.3f} over {diff.shape[0]} rows")
-    assert np.all(np.isfinite(q8))
-    assert diff.max() > 0.0
+    return float(diff.max()), float(np.sqrt((diff ** 2).mean())), float(ref[1:].std()), agree, \
+        diff.shape[0]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["qwen3_8b_b1", "dflash2_b16"])
+def test_fp8_context_study(name):
+    """Draft logits with the context K/V in bf16 and in fp8 for the first
+    request of the Qwen3-8B-shaped batch-1 and the DFlash-2 workloads.
+    Prints the measured change; asserts only that the fp8 cache perturbs the
+    logits (it is a lossy format) and keeps every logit finite."""
+    mx, rms, std, agree, rows = fp8_study(name)
+    print(f"\nfp8 context K/V, {name}: max|dlogit| {mx:.4f}, rms {rms:.5f}, "
+          f"logit std {std:.3f}, top-1 agreement {agree:.3f} over {rows} rows")
+    assert mx > 0.0
