@@ -14,7 +14,7 @@ Source passages (cited by page title and section):
   [P3] "NVIDIA tests DFlash to cut LLM inference bottlenecks"
        (stechtimes.com), section "DFlash moves drafting to parallel compute".
 
-Readings of points the pages leave open (each also listed in the design doc):
+Readings of points the pages leave open:
   R1 pre-norm RMSNorm decoder layers, SwiGLU MLP, GQA with per-head q/k
      RMSNorm before rotate-half RoPE (Qwen3-shaped);
   R2 a tap is the residual-stream output of a 0-indexed target layer;
