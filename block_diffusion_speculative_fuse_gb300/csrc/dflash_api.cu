@@ -661,6 +661,22 @@ int check_cfg(const dflash_config* c, bool draft) {
 
 }  // namespace
 
+namespace dflash {
+// Argument and capacity checks of dflash_ctx_fuse (nothing is launched).
+int ctx_fuse_check(const dflash_model_s* m, const void* taps, int32_t T, const void* ctx,
+                   const void* ws, size_t ws_bytes) {
+  if (m == nullptr || !m->is_draft || taps == nullptr || ctx == nullptr || ws == nullptr || T < 1)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(taps) || !aligned16(ctx) || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return DFLASH_ERR_INVALID_ARG;
+  Ws w;
+  w.dry = true;
+  w.take<float>(partial_floats(m, 0, T));
+  w.take<float>(static_cast<size_t>(T) * m->cfg.hidden);
+  return w.off > ws_bytes ? DFLASH_ERR_CAPACITY : DFLASH_OK;
+}
+}  // namespace dflash
+
 // ======================================================================= ABI
 extern "C" {
 
@@ -816,17 +832,14 @@ int dflash_get_status(const void* ws, int32_t* status, int32_t* site, void* stre
 
 int dflash_ctx_fuse(dflash_model m, const void* taps, int32_t T, void* ctx, void* ws,
                     size_t ws_bytes, void* stream) {
-  if (m == nullptr || !m->is_draft || taps == nullptr || ctx == nullptr || ws == nullptr || T < 1)
-    return DFLASH_ERR_INVALID_ARG;
-  if (!aligned16(taps) || !aligned16(ctx) || (reinterpret_cast<uintptr_t>(ws) & 255))
-    return DFLASH_ERR_INVALID_ARG;
+  int rc = dflash::ctx_fuse_check(m, taps, T, ctx, ws, ws_bytes);
+  if (rc) return rc;
   const dflash_config& c = m->cfg;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Ws w;
   w.base = static_cast<uint8_t*>(ws);
   float* partial = w.take<float>(partial_floats(m, 0, T));
   float* cf = w.take<float>(static_cast<size_t>(T) * c.hidden);
-  if (w.off > ws_bytes) return DFLASH_ERR_CAPACITY;
   const int K = c.n_taps * c.hidden;
   GemmParams p = gemm_base(m, T, c.hidden, K, gemm_bn_for(T), w);
   if (c.fc_norm) {
@@ -837,7 +850,7 @@ int dflash_ctx_fuse(dflash_model m, const void* taps, int32_t T, void* ctx, void
     p.out = ctx;
   }
   p.ld_out = c.hidden;
-  int rc = run_gemm(m, &m->m_fc, taps, K, p, partial, s);
+  rc = run_gemm(m, &m->m_fc, taps, K, p, partial, s);
   if (rc) return rc;
   if (c.fc_norm)
     DF_CUDA(rmsnorm_launch(cf, T, c.hidden, u16(m->w.fc_norm), c.rms_eps,

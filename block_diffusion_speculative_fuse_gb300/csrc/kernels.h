@@ -5,11 +5,18 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+struct dflash_model_s;
+
 namespace dflash {
 
 constexpr int kTileN = 128;      // weight rows per CTA tile (MMA M)
 constexpr int kTileK = 64;       // K elements per pipeline stage (one 128-B swizzle row)
 constexpr int kMaxRopePairs = 64;
+
+// Argument and workspace-capacity checks of dflash_ctx_fuse; returns the
+// DFLASH_* code the call would return before launching anything.
+int ctx_fuse_check(const dflash_model_s* m, const void* taps, int32_t T, const void* ctx,
+                   const void* ws, size_t ws_bytes);
 
 // Host-side count of kernel launches issued by this library.
 uint64_t launch_count();

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "dflash.h"
+#include "kernels.h"
 
 namespace {
 
@@ -24,7 +25,9 @@ std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device (looked up once
-// per device; the host-side symbol itself is not a device address).
+// per device; the host-side symbol itself is not a device address).  The
+// cached address belongs to the device's primary context: it is not looked
+// up again after that context is destroyed (cudaDeviceReset).
 int scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -48,9 +51,13 @@ extern "C" int dflash_ctx_fuse_noalloc(dflash_model m, const void* taps, int32_t
   void* scratch = nullptr;
   int rc = scratch_for_current_device(&scratch);
   if (rc) return rc;
+  // Reject bad arguments and T beyond what fits in the fixed scratch
+  // (DFLASH_ERR_CAPACITY) before touching the shared array, so that a call
+  // that launches nothing does not clear the header under a call in flight.
+  rc = dflash::ctx_fuse_check(m, taps, T, ctx, scratch, kNoAllocScratchBytes);
+  if (rc) return rc;
   // the header (status word, split counters) must start at zero every call
   rc = dflash_workspace_init(scratch, kNoAllocScratchBytes, stream);
   if (rc) return rc;
-  // T beyond what fits in the fixed scratch is rejected with DFLASH_ERR_CAPACITY
   return dflash_ctx_fuse(m, taps, T, ctx, scratch, kNoAllocScratchBytes, stream);
 }

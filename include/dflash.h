@@ -179,12 +179,16 @@ int dflash_kv_append(dflash_model m, const void* ctx, const int32_t* row_req,
  * Same inputs and output as dflash_ctx_fuse, no workspace argument: the
  * scratch is a fixed 4 MiB array inside the library, held by every GPU that
  * loads the library until the process exits.  Needs 64 KiB + T*hidden*4 bytes
- * of it (T <= 240 at hidden 4096); larger T returns DFLASH_ERR_CAPACITY.
+ * of it, so T <= (4 MiB - 64 KiB) / (hidden*4): 252 rows at hidden 4096,
+ * 2016 at hidden 512.  A larger T, like any other bad argument, is rejected
+ * (DFLASH_ERR_CAPACITY) before the array is touched or anything is launched.
  * The first call on a device looks up the array's device address; make that
- * first call before any stream capture.  All calls share the array (the
- * header is cleared at the start of each call), so calls that may overlap on
- * the GPU (different streams, or devices sharing a context) race.  Device-side
- * status is not reported back. */
+ * first call before any stream capture.  The address is kept for the device's
+ * primary context: after that context is destroyed (cudaDeviceReset) it is
+ * stale, and this call must not be used again in the process.  All calls
+ * share the array (the header is cleared at the start of each call that
+ * launches), so calls that may overlap on the GPU (different streams, or
+ * devices sharing a context) race.  Device-side status is not reported back. */
 int dflash_ctx_fuse_noalloc(dflash_model m, const void* taps, int32_t T, void* ctx,
                             void* stream);
 

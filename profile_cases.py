@@ -1,7 +1,7 @@
 """Small, self-contained launch cases for profiling single kernels with ncu.
 
-    python -m block_diffusion_speculative_fuse_gb300.profile_cases lm_head
-    python -m block_diffusion_speculative_fuse_gb300.profile_cases step [--config NAME]
+    python profile_cases.py lm_head
+    python profile_cases.py step [--config NAME]
 
 lm_head: the shared LM head + argmax of the Qwen3-8B-shaped drafter
 (151936 x 4096 bf16 weights, 16 rows), launched a few times, ~1.7 GB on the
@@ -14,14 +14,14 @@ import sys
 import numpy as np
 import torch
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 import workload as W  # noqa: E402
 
-from . import _build, binding as B  # noqa: E402
-from .device import DeviceModel, to_device_u16  # noqa: E402
+from block_diffusion_speculative_fuse_gb300 import _build, binding as B  # noqa: E402
+from block_diffusion_speculative_fuse_gb300.device import DeviceModel, to_device_u16  # noqa: E402
 
 
 def lm_head(iters=3, rows=16):
@@ -41,7 +41,7 @@ def lm_head(iters=3, rows=16):
 
 
 def step(config="qwen3_8b_b1", iters=3):
-    from .session import DraftStep
+    from block_diffusion_speculative_fuse_gb300.session import DraftStep
     st = DraftStep(W.get_workload(config))
     for _ in range(iters):
         st.step()

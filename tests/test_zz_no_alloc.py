@@ -62,3 +62,29 @@ def test_noalloc_rejects_oversize():
     with pytest.raises(B.DflashError) as e:
         B.dflash_ctx_fuse_noalloc(m.handle, taps, T, out)
     assert e.value.code == -3
+
+
+def test_noalloc_capacity_edge():
+    """The largest T that fits the 4 MiB array works and matches the workspace
+    fuse; one row more is rejected before anything runs, and the array still
+    gives correct results afterwards."""
+    from block_diffusion_speculative_fuse_gb300 import binding as B
+    from block_diffusion_speculative_fuse_gb300.device import DeviceModel, to_device_u16
+    H = 512
+    wl = tiny_workload("noalloc_edge", wid=897, hidden=H, n_q_heads=8, n_kv_heads=4,
+                       head_dim=64, mlp=256, vocab=256, n_taps=2)
+    d = wl.draft
+    m = DeviceModel(d, W.draft_weights(d, wl.wid), W.shared_weights(d, wl.wid), draft=True)
+    t_max = ((4 << 20) - (64 << 10)) // (H * 4)   # 2016 rows
+    taps = to_device_u16(W.taps_bf16(t_max + 1, d, wl.wid))
+    ref = torch.zeros((t_max, H), dtype=torch.bfloat16, device="cuda")
+    ws = m.workspace(d.block, t_max, 1, 16)
+    B.dflash_ctx_fuse(m.handle, taps, t_max, ref, ws)
+    out = torch.zeros((t_max + 1, H), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.DflashError) as e:
+        B.dflash_ctx_fuse_noalloc(m.handle, taps, t_max + 1, out)
+    assert e.value.code == -3
+    B.dflash_ctx_fuse_noalloc(m.handle, taps, t_max, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out[:t_max].float().cpu().numpy(), ref.float().cpu().numpy())
+    assert not out[t_max].float().abs().sum().item()  # the row past T is untouched
