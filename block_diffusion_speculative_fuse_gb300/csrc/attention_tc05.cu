@@ -133,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // both P buffers start at zero: rows that no thread writes stay zero
   for (int idx = tid; idx < 2 * C::P_BYTES / 16; idx += kThreads)
     *reinterpret_cast<uint4*>(sm + C::P_OFF + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
-  griddep_launch_dependents();
+  // The next kernel may launch once every CTA has issued its key loads (the
+  // producer signals below), so that its early weight loads queue behind them.
   griddep_wait();
 
   // ---- one round of global loads, all issued before any is used: the
@@ -245,7 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(dst, map, hf * 64, y, &kv_full[st], pol);
       }
       ++issued;
+      if (c == min(nch, kStages) - 1) griddep_launch_dependents();
     }
+    if (nch == 0 || issued < min(nch, kStages)) griddep_launch_dependents();  // none issued, or an abort
     // copies still in flight after an abort land before the CTA exits
     if (lane == 0)
       for (int c = max(0, issued - kStages); c < issued; ++c)

@@ -77,6 +77,9 @@ struct dflash_model_s {
   bool is_draft = false;
   bool persistent = false;  // use the persistent layer-stack kernel when the shape allows
   bool attn_tc = true;      // drafter attention on tcgen05 (attention_tc05.cu) when the shape allows
+  // GEMM: k-blocks its producer still has to request when the next kernel
+  // may launch (< 0: at the start)
+  int dep_lead = 2;
   CUtensorMap m_wqkv, m_wo, m_gu, m_down, m_lm, m_fc;
   float2 rope[kMaxRopePairs];
   int qkv_rows = 0, q_dim = 0, kv_dim = 0;
@@ -84,8 +87,14 @@ struct dflash_model_s {
 
 namespace {
 
-constexpr size_t kHeaderBytes = 64 * 1024;       // status word + split counters
-constexpr int kMaxCounters = (kHeaderBytes - 256) / 4;
+// Workspace header (zeroed by dflash_workspace_init; every kernel leaves
+// what it uses at zero): [0, 256) status word (int32 [0] code, [1] site, [2]
+// LM-head argmax ticket), [256, 32 KiB) split-K counters, [32 KiB, 64 KiB)
+// LM-head argmax keys (uint64 per row).
+constexpr size_t kHeaderBytes = 64 * 1024;
+constexpr size_t kAmaxKeyOff = 32 * 1024;
+constexpr int kMaxCounters = (kAmaxKeyOff - 256) / 4;
+constexpr int kMaxAmaxKeyRows = static_cast<int>((kHeaderBytes - kAmaxKeyOff) / 8);
 constexpr int kTargetSplitKeys = 512;
 constexpr int kMaxClusterSplits = 8;  // portable cluster size
 
@@ -120,6 +129,9 @@ struct Ws {
   }
   int32_t* status() const { return dry ? nullptr : reinterpret_cast<int32_t*>(base); }
   int32_t* counters() const { return dry ? nullptr : reinterpret_cast<int32_t*>(base + 256); }
+  unsigned long long* amax_keys() const {
+    return dry ? nullptr : reinterpret_cast<unsigned long long*>(base + kAmaxKeyOff);
+  }
 };
 
 // Buffers of one stack pass over `rows` activation rows (+ ctx rows on the QKV input).
@@ -240,6 +252,7 @@ GemmParams gemm_base(const dflash_model_s* m, int M, int N, int K, int bn, Ws& w
   p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;
   p.counters = ws.counters();
   p.status = ws.status();
+  p.dep_lead = m->dep_lead;
   return p;
 }
 
@@ -605,10 +618,20 @@ int run_lm_head(const dflash_model_s* m, Ws& ws, StackBufs& b, int rows, int blo
   if (b.ssq_a2 != nullptr) set_norm_in(m, p, b.ssq_a2, rows);
   p.splits = 1;  // argmax needs the full dot product per tile
   p.kb_per_split = p.kb_total;
+  const bool fused = rows <= kMaxAmaxKeyRows;
+  if (fused) {
+    // the cross-tile argmax finishes inside the GEMM launch
+    p.amax_key = ws.amax_keys();
+    p.amax_ticket = ws.status() + 2;
+    p.amax_out = out;
+    p.amax_block = block;
+    p.amax_skip_first = skip_first;
+  }
   int rc = run_gemm(m, &m->m_lm, b.a2, c.hidden, p, b.partial, s);
   if (rc) return rc;
-  DF_CUDA(argmax_reduce_launch(b.amax_val, b.amax_idx, rows, c.vocab / kTileN, block, out,
-                               skip_first, s, true));
+  if (!fused)
+    DF_CUDA(argmax_reduce_launch(b.amax_val, b.amax_idx, rows, c.vocab / kTileN, block, out,
+                                 skip_first, s, true));
   return DFLASH_OK;
 }
 
@@ -736,6 +759,10 @@ int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflas
     // DFLASH_ATTN_TC=0 keeps the drafter on the mma.sync attention kernel
     const char* t = std::getenv("DFLASH_ATTN_TC");
     m->attn_tc = !(t != nullptr && t[0] == '0');
+    // DFLASH_DEP_LEAD=k: a GEMM lets the next kernel launch when its producer
+    // has k weight k-blocks left to request (-1: at the start)
+    const char* dl = std::getenv("DFLASH_DEP_LEAD");
+    if (dl != nullptr && dl[0] != 0) m->dep_lead = std::atoi(dl);
   }
   if (draft && m->attn_tc && (cfg->head_dim == 64 || cfg->head_dim == 128))
     attention_tc_prepare(cfg->head_dim);

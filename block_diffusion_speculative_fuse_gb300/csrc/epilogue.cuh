@@ -34,6 +34,22 @@ __device__ __forceinline__ void rope_sincos(int pos, float2 f, float* s, float* 
   sincosf(r, s, c);
 }
 
+// ---------------------------------------------------------------- argmax keys
+// (value, index) as one unsigned 64-bit key whose integer order is: larger
+// value first, then lower index.  The value's bits are mapped to an unsigned
+// integer of the same order (negative: all bits flipped; otherwise the sign
+// bit set); -0 is taken as +0 so that the two zeros tie like in a float
+// comparison.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+  if (v == 0.f) v = 0.f;
+  const uint32_t b = __float_as_uint(v);
+  const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<unsigned long long>(o) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(idx));
+}
+__device__ __forceinline__ int argmax_key_index(unsigned long long k) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+}
+
 // ---------------------------------------------------------------- epilogues
 template <typename Sync>
 __device__ void epi_store(const GemmParams& p, const float* ts, int tile, int m0, int rows,
@@ -161,8 +177,12 @@ __device__ void epi_argmax(const GemmParams& p, const float* ts, int tile, int m
         if (v.z > bv) { bv = v.z; bi = n0 + 4 * c4 + 2; }
         if (v.w > bv) { bv = v.w; bi = n0 + 4 * c4 + 3; }
       }
-      p.amax_val[static_cast<size_t>(m0 + r) * n_tiles + tile] = bv;
-      p.amax_idx[static_cast<size_t>(m0 + r) * n_tiles + tile] = bi;
+      if (p.amax_key != nullptr) {
+        atomicMax(p.amax_key + m0 + r, argmax_key(bv, bi));
+      } else {
+        p.amax_val[static_cast<size_t>(m0 + r) * n_tiles + tile] = bv;
+        p.amax_idx[static_cast<size_t>(m0 + r) * n_tiles + tile] = bi;
+      }
     }
   }
   for (int r = warp; r < (rows > 32 ? 0 : rows); r += 4) {
@@ -181,8 +201,12 @@ __device__ void epi_argmax(const GemmParams& p, const float* ts, int tile, int m
       if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
     }
     if (lane == 0) {
-      p.amax_val[static_cast<size_t>(m0 + r) * n_tiles + tile] = bv;
-      p.amax_idx[static_cast<size_t>(m0 + r) * n_tiles + tile] = bi;
+      if (p.amax_key != nullptr) {
+        atomicMax(p.amax_key + m0 + r, argmax_key(bv, bi));
+      } else {
+        p.amax_val[static_cast<size_t>(m0 + r) * n_tiles + tile] = bv;
+        p.amax_idx[static_cast<size_t>(m0 + r) * n_tiles + tile] = bi;
+      }
     }
   }
   if (p.logits != nullptr) {

@@ -99,7 +99,11 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  griddep_launch_dependents();
+  // The next kernel may launch once every CTA has signalled: at the start
+  // (dep_lead < 0), or when this CTA's producer has dep_lead k-blocks left to
+  // request, so that the next kernel's early weight loads follow this one's
+  // instead of competing with them.
+  if (p.dep_lead < 0 || nkb <= 0) griddep_launch_dependents();
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -107,7 +111,9 @@ __global__ void __launch_bounds__(128, 1)
     const uint64_t pol_x = l2_policy_evict_last();
     const int wrow = p.w_row0 + tile * p.w_tile_step;
     const int pre = nkb < C::STAGES ? nkb : C::STAGES;
+    const int dep_it = p.dep_lead < 0 ? -1 : max(0, nkb - 1 - p.dep_lead);
     for (int it = 0; it < pre; ++it) {
+      if (it == dep_it) griddep_launch_dependents();
       uint8_t* a = smem + it * C::A_BYTES;
       const int kx = (kb0 + it) * kTileK;
       mbar_arrive_expect_tx(&full[it], C::STAGE_BYTES);
@@ -126,8 +132,10 @@ __global__ void __launch_bounds__(128, 1)
       if (!mbar_wait(&empty[s], ph, abort_flag)) {
         *abort_flag = 1;
         raise_status(p.status, DFLASH_ERR_TIMEOUT, 11);
+        griddep_launch_dependents();
         break;
       }
+      if (it == dep_it) griddep_launch_dependents();
       uint8_t* a = smem + s * C::A_BYTES;
       uint8_t* b = smem + C::STAGES * C::A_BYTES + s * C::B_STAGE;
       const int kx = (kb0 + it) * kTileK;
@@ -416,6 +424,29 @@ __global__ void __launch_bounds__(128, 1)
                 tid, sync);
         break;
       default: break;
+    }
+  }
+  if (p.mode == EPI_ARGMAX && p.amax_key != nullptr) {
+    // the last CTA to finish turns the per-row keys into tokens (no waiting:
+    // every other CTA has folded its keys in before taking its ticket)
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const int n_ctas = gridDim.x * gridDim.y * gridDim.z;
+      *last_flag = (atomicAdd(p.amax_ticket, 1) == n_ctas - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (*last_flag) {
+      __threadfence();
+      for (int r = tid; r < p.M; r += 128) {
+        const int idx = argmax_key_index(atomicExch(p.amax_key + r, 0ull));
+        const int i = r % p.amax_block;
+        if (!p.amax_skip_first)
+          p.amax_out[r] = idx;
+        else if (i != 0)
+          p.amax_out[(r / p.amax_block) * (p.amax_block - 1) + i - 1] = idx;
+      }
+      if (tid == 0) *p.amax_ticket = 0;
     }
   }
   if (p.splits > 1 && p.cluster && !push) cluster_sync();  // peers may still read this CTA's tile until here

@@ -81,6 +81,15 @@ struct GemmParams {
   int ld_logits;
   float* amax_val;       // [M][n_tiles]
   int32_t* amax_idx;
+  // Argmax finished inside the LM-head launch (amax_key != null): every CTA
+  // folds its per-row (max, lowest index) into amax_key[m] with a 64-bit
+  // atomic max, and the CTA that takes the last ticket writes the tokens to
+  // amax_out (rows i % amax_block == 0 skipped when amax_skip_first: row m
+  // goes to (m / B) * (B - 1) + i - 1) and clears the keys and the ticket.
+  unsigned long long* amax_key;  // [M], zero between launches
+  int32_t* amax_ticket;          // zero between launches
+  int32_t* amax_out;
+  int amax_block, amax_skip_first;
   // Deferred RMSNorm of the input rows: rows m < norm_rows of the result are
   // scaled by 1/sqrt(sum_t ssq_in[m][t] / norm_dim + norm_eps) (the input
   // operand holds bf16(x * g), the producer wrote per-tile sums of x^2).
@@ -97,6 +106,7 @@ struct GemmParams {
   uint16_t* raw_out;
   int ld_raw;
   QkvEpi qkv;
+  int dep_lead;          // < 0: signal dependents at the start; else with dep_lead k-blocks left to load
 };
 
 // Picks the MMA N width for M rows and the split-K count.
