@@ -1,5 +1,4 @@
-// Attention building blocks shared by the attention kernels (attention.cu)
-// and the persistent layer-stack kernel (persistent_stack.cu).
+// Attention building blocks of the mma.sync attention kernel (attention.cu).
 #pragma once
 #include "common.cuh"
 #include "kernels.h"
@@ -122,7 +121,7 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const int c = kk * 16 + tq * 2;
-      // L2-coherent loads: inside the persistent kernel q is rewritten every layer
+      // L2-coherent loads (q was written by the previous kernel)
       qf[kk][0] = v0 ? __ldcg(reinterpret_cast<const unsigned int*>(q0 + c)) : 0u;
       qf[kk][1] = v1 ? __ldcg(reinterpret_cast<const unsigned int*>(q1 + c)) : 0u;
       qf[kk][2] = v0 ? __ldcg(reinterpret_cast<const unsigned int*>(q0 + c + 8)) : 0u;

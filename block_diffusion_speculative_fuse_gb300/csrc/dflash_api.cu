@@ -75,7 +75,6 @@ struct dflash_model_s {
   int device = 0;
   int sms = 148;
   bool is_draft = false;
-  bool persistent = false;  // use the persistent layer-stack kernel when the shape allows
   bool attn_tc = true;      // drafter attention on tcgen05 (attention_tc05.cu) when the shape allows
   // GEMM: k-blocks its producer still has to request when the next kernel
   // may launch (< 0: at the start)
@@ -157,7 +156,6 @@ struct StackBufs {
   float* ctx_f32;
   float* ssq_a;    // [rows][H/128] per-tile sums of squares of the rows behind `a`
   float* ssq_a2;   // same for `a2`
-  float* persist_part;  // stream-K partial tiles of the persistent kernel
 };
 
 struct GemmShape {
@@ -203,9 +201,6 @@ int attn_n_splits(const dflash_model_s* m, int split_keys, int max_keys) {
   return m->is_draft ? n + 1 : std::max(1, n);
 }
 
-bool persistent_ok(const dflash_model_s* m, int rows, int T);
-size_t persist_part_floats_for(const dflash_model_s* m);
-PersistParams persist_dims(const dflash_model_s* m);
 
 void layout_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n, int ctx_rows,
                   int max_keys) {
@@ -233,8 +228,6 @@ void layout_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int 
   b.ctx_f32 = nullptr;
   b.ssq_a = ws.take<float>(static_cast<size_t>(rows) * (c.hidden / kTileN));
   b.ssq_a2 = ws.take<float>(static_cast<size_t>(rows) * (c.hidden / kTileN));
-  b.persist_part = persistent_ok(m, rows, ctx_rows) ? ws.take<float>(persist_part_floats_for(m))
-                                                    : nullptr;
 }
 
 GemmParams gemm_base(const dflash_model_s* m, int M, int N, int K, int bn, Ws& ws) {
@@ -499,113 +492,6 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
   return DFLASH_OK;
 }
 
-// Draft stack + LM head + argmax in the persistent kernel (after the embed
-// kernel).  Returns DFLASH_ERR_UNSUPPORTED (nothing launched but the embed) if
-// the device cannot co-schedule one CTA per SM.
-int run_persistent(dflash_model_s* m, Ws& w, StackBufs& b, int batch, const int32_t* anchor,
-                   const int32_t* anchor_pos, const dflash_kv* kv, const void* pending_ctx,
-                   const int32_t* pending_req, const int32_t* pending_pos, int T, int32_t* draft,
-                   float* logits, cudaStream_t s) {
-  const dflash_config& c = m->cfg;
-  const int B = c.block, rows = batch * B, H = c.hidden;
-  const int max_keys = kv->max_pages * c.page_size;
-  PersistParams P = persist_dims(m);
-  P.nb = rows;
-  P.M_qkv = rows + T;
-  P.block = B;
-  P.conv_width = c.conv_width;
-  P.eps = c.rms_eps;
-  P.in_norm = u16(m->w.in_norm);
-  P.post_norm = u16(m->w.post_norm);
-  P.final_norm = u16(m->w.final_norm);
-  P.conv = c.conv_width > 0 ? u16(m->w.conv) : nullptr;
-  P.pool = static_cast<uint16_t*>(kv->pool);
-  P.pool_layer_elems = layer_pool_elems(m, kv);
-  P.part = b.persist_part;
-  P.x = b.x;
-  P.a = b.a;
-  P.a2 = b.a2;
-  P.hmid = b.hmid;
-  P.ssq_a = b.ssq_a;
-  P.ssq_a2 = b.ssq_a2;
-  P.amax_val = b.amax_val;
-  P.amax_idx = b.amax_idx;
-  P.draft = draft;
-  P.logits = logits;
-  P.bar = reinterpret_cast<unsigned*>(w.counters());
-  P.status = w.status();
-  P.m_wqkv = m->m_wqkv;
-  P.m_wo = m->m_wo;
-  P.m_gu = m->m_gu;
-  P.m_down = m->m_down;
-  P.m_lm = m->m_lm;
-  int rc = encode_map(&P.x_a, b.a, rows + T, H, H, 32);
-  if (!rc) rc = encode_map(&P.x_o, b.o, rows, m->q_dim, m->q_dim, 32);
-  if (!rc) rc = encode_map(&P.x_a2, b.a2, rows, H, H, 32);
-  if (!rc) rc = encode_map(&P.x_h, b.hmid, rows, c.mlp, c.mlp, 32);
-  if (rc) return rc;
-  // epilogue template
-  GemmParams& e = P.ep;
-  std::memset(&e, 0, sizeof(e));
-  e.status = w.status();
-  e.resid = b.x;
-  e.ld_resid = H;
-  e.ld_xg = H;
-  e.ssq_ld = H / kTileN;
-  e.block = B;
-  e.amax_val = b.amax_val;
-  e.amax_idx = b.amax_idx;
-  e.logits = logits;
-  e.ld_logits = c.vocab;
-  QkvEpi q = qkv_base(m, 0);
-  set_pool(m, q, kv, 0);
-  q.q = b.q;
-  q.n_blk = rows;
-  q.block = B;
-  q.anchor_pos = anchor_pos;
-  q.pool_req = pending_req;
-  q.pool_pos = pending_pos;
-  q.keep_q_pool = 0;
-  q.kblk = b.kblk;
-  q.vblk = b.vblk;
-  e.qkv = q;
-  // attention template
-  AttnParams& a = P.att;
-  std::memset(&a, 0, sizeof(a));
-  a.q = b.q;
-  a.batch = batch;
-  a.n = B;
-  a.pos0 = anchor_pos;
-  a.causal = 0;
-  a.page_table = kv->page_table;
-  a.max_pages = kv->max_pages;
-  a.n_pages = kv->n_pages;
-  a.page_size = c.page_size;
-  a.kblk = b.kblk;
-  a.vblk = b.vblk;
-  a.hq = c.n_q_heads;
-  a.hkv = c.n_kv_heads;
-  a.d = c.head_dim;
-  a.split_keys = attn_split_keys(m, batch, max_keys);
-  a.n_splits = attn_n_splits(m, a.split_keys, max_keys);
-  a.cluster = 0;
-  a.o_part = b.o_part;
-  a.ml_part = b.ml_part;
-  a.out = b.o;
-  a.status = w.status();
-  DF_CUDA(embed_block_launch(anchor, batch, B, u16(m->w.embed), u16(m->w.mask_embed),
-                             u16(m->w.in_norm), H, b.x, b.a, H, b.ssq_a, u16(pending_ctx), T, s,
-                             true, w.status(), c.vocab, P.bar));
-  cudaError_t err = persistent_launch(P, persistent_ctas(P, m->sms), s);
-  if (err == cudaErrorCooperativeLaunchTooLarge) {
-    cudaGetLastError();
-    m->persistent = false;
-    return DFLASH_ERR_UNSUPPORTED;
-  }
-  if (err != cudaSuccess) return cuda_fail(err);
-  return DFLASH_OK;
-}
-
 int run_lm_head(const dflash_model_s* m, Ws& ws, StackBufs& b, int rows, int block,
                 int skip_first, int32_t* out, float* logits, cudaStream_t s) {
   const dflash_config& c = m->cfg;
@@ -635,35 +521,11 @@ int run_lm_head(const dflash_model_s* m, Ws& ws, StackBufs& b, int rows, int blo
   return DFLASH_OK;
 }
 
-// The persistent layer-stack kernel covers decode-sized draft steps.
-bool persistent_ok(const dflash_model_s* m, int rows, int T) {
-  const dflash_config& c = m->cfg;
-  return m->persistent && m->is_draft && c.block >= 2 && rows + T <= 32 &&
-         (c.head_dim == 64 || c.head_dim == 128) && c.n_q_heads / c.n_kv_heads <= 4;
-}
-
-PersistParams persist_dims(const dflash_model_s* m) {
-  PersistParams p;
-  std::memset(static_cast<void*>(&p), 0, sizeof(p));
-  const dflash_config& c = m->cfg;
-  p.n_layers = c.n_layers;
-  p.H = c.hidden;
-  p.F = c.mlp;
-  p.V = c.vocab;
-  p.q_dim = m->q_dim;
-  p.kv_dim = m->kv_dim;
-  p.qkv_rows = m->qkv_rows;
-  p.head_dim = c.head_dim;
-  return p;
-}
-
-size_t persist_part_floats_for(const dflash_model_s* m) {
-  const PersistParams d = persist_dims(m);
-  return persistent_part_floats(d, persistent_ctas(d, m->sms));
-}
-
 int check_cfg(const dflash_config* c, bool draft) {
-  if (c->n_layers < 1 || c->hidden < 128 || c->hidden % 128 || c->vocab < 128 || c->vocab % 128)
+  // hidden <= 8192: the row kernels hold a row in registers (8 columns x 4
+  // chunks per thread of 256)
+  if (c->n_layers < 1 || c->hidden < 128 || c->hidden % 128 || c->hidden > 8192 ||
+      c->vocab < 128 || c->vocab % 128)
     return DFLASH_ERR_UNSUPPORTED;
   if (c->head_dim != 64 && c->head_dim != 128) return DFLASH_ERR_UNSUPPORTED;
   if (c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads) return DFLASH_ERR_UNSUPPORTED;
@@ -732,7 +594,8 @@ int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflas
     if (p == nullptr || !aligned16(p)) return DFLASH_ERR_INVALID_ARG;
   if (cfg->qk_norm && (w->q_norm == nullptr || w->k_norm == nullptr)) return DFLASH_ERR_INVALID_ARG;
   if (draft && (w->fc == nullptr || w->mask_embed == nullptr || !aligned16(w->fc) ||
-                (cfg->fc_norm && w->fc_norm == nullptr)))
+                !aligned16(w->mask_embed) ||
+                (cfg->fc_norm && (w->fc_norm == nullptr || !aligned16(w->fc_norm)))))
     return DFLASH_ERR_INVALID_ARG;
   if (draft && cfg->conv_width > 0 && w->conv == nullptr) return DFLASH_ERR_INVALID_ARG;
 
@@ -752,10 +615,6 @@ int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflas
   m->sms = prop.multiProcessorCount;
   m->is_draft = draft;
   {
-    // The persistent layer-stack kernel is opt-in (DFLASH_PERSISTENT=1): on
-    // the Qwen3-8B-shaped step it measured slower than the per-GEMM kernels.
-    const char* e = std::getenv("DFLASH_PERSISTENT");
-    m->persistent = (e != nullptr && e[0] == '1');
     // DFLASH_ATTN_TC=0 keeps the drafter on the mma.sync attention kernel
     const char* t = std::getenv("DFLASH_ATTN_TC");
     m->attn_tc = !(t != nullptr && t[0] == '0');
@@ -815,18 +674,14 @@ size_t dflash_workspace_bytes(dflash_model m, int32_t max_block_rows, int32_t ma
     StackBufs b;
     const int n = std::max(1, max_block_rows / max_batch);
     layout_stack(m, ws, b, max_batch, n, max_ctx_rows, max_keys);
-    // the attention partials are sized for the worst split count over batch
-    // sizes; calls with few enough rows also take the persistent kernel
+    // the attention partials are sized for the worst split count over batch sizes
     for (int bt = 1; bt <= max_batch; bt *= 2) {
       const int nb = std::max(1, max_block_rows / bt);
-      const int t_pers = std::max(0, std::min(max_ctx_rows, 32 - bt * nb));
-      for (int ctx : {max_ctx_rows, t_pers}) {
-        Ws w2;
-        w2.dry = true;
-        StackBufs b2;
-        layout_stack(m, w2, b2, bt, nb, ctx, max_keys);
-        need = std::max(need, w2.off);
-      }
+      Ws w2;
+      w2.dry = true;
+      StackBufs b2;
+      layout_stack(m, w2, b2, bt, nb, max_ctx_rows, max_keys);
+      need = std::max(need, w2.off);
     }
     need = std::max(need, ws.off);
   }
@@ -941,16 +796,6 @@ int dflash_draft_block(dflash_model m, const int32_t* anchor, const int32_t* anc
   const int max_keys = kv->max_pages * c.page_size;
   layout_stack(m, w, b, batch, B, T, max_keys);
   if (w.off > ws_bytes) return DFLASH_ERR_CAPACITY;
-  if (b.persist_part != nullptr) {
-    rc = run_persistent(m, w, b, batch, anchor, anchor_pos, kv, pending_ctx, pending_req,
-                        pending_pos, T, draft, logits, s);
-    if (rc == DFLASH_OK) {
-      if (hidden != nullptr)
-        DF_CUDA(copy_rows_f32_launch(b.x, hidden, static_cast<size_t>(rows) * c.hidden, s, true));
-      return DFLASH_OK;
-    }
-    if (rc != DFLASH_ERR_UNSUPPORTED) return rc;
-  }
   DF_CUDA(embed_block_launch(anchor, batch, B, u16(m->w.embed), u16(m->w.mask_embed),
                              u16(m->w.in_norm), c.hidden, b.x, b.a, c.hidden, b.ssq_a,
                              u16(pending_ctx), T, s, true, w.status(), c.vocab));

@@ -1,5 +1,4 @@
-// Fused GEMM epilogues, shared by the per-GEMM kernel (gemm_tc05.cu) and the
-// persistent layer-stack kernel (persistent_stack.cu).  Each works on a staged
+// Fused GEMM epilogues of the tcgen05 GEMM (gemm_tc05.cu).  Each works on a staged
 // fp32 tile ts[rows][kTsLd] (rows = activation rows, 128 output features) with
 // 128 cooperating threads (local index tid, 0..127, warp-aligned) and a
 // caller-supplied barrier over those threads.
@@ -66,22 +65,29 @@ __device__ void epi_store(const GemmParams& p, const float* ts, int tile, int m0
   }
 }
 
+// pre_resid (nullable): the residual rows m0 .. m0+rows-1 of this tile's 128
+// columns, already loaded ([rows][128]); pre_g (nullable): gnext of the tile.
 template <typename Sync>
 __device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int rows,
-                          int tid, Sync sync) {
+                          int tid, Sync sync, const float* pre_resid = nullptr,
+                          const float* pre_g = nullptr) {
     // Thread f owns feature column n0 + f: x_new = x + acc, then the optional
   // depthwise conv along block positions (sliding window down the column,
   // zero padded at each request's block edges), then the next norm's inputs.
   const int f = tid;
   const int n = tile * kTileN + f;
-  for (int r0 = 0; r0 < rows; r0 += 16) {
-    float v[16];
+  if (pre_resid != nullptr) {
+    for (int r = 0; r < rows; ++r) ts[r * kTsLd + f] += pre_resid[r * kTileN + f];
+  } else {
+    for (int r0 = 0; r0 < rows; r0 += 16) {
+      float v[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      v[j] = (r0 + j < rows) ? __ldcg(p.resid + static_cast<size_t>(m0 + r0 + j) * p.ld_resid + n) : 0.f;
+      for (int j = 0; j < 16; ++j)
+        v[j] = (r0 + j < rows) ? __ldcg(p.resid + static_cast<size_t>(m0 + r0 + j) * p.ld_resid + n) : 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (r0 + j < rows) ts[(r0 + j) * kTsLd + f] += v[j];
+      for (int j = 0; j < 16; ++j)
+        if (r0 + j < rows) ts[(r0 + j) * kTsLd + f] += v[j];
+    }
   }
   if (p.conv != nullptr && p.conv_width > 0) {
     const int c = (p.conv_width - 1) / 2;
@@ -113,12 +119,13 @@ __device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int 
       }
     }
   }
+  const float gn = p.xg_out == nullptr ? 0.f : (pre_g != nullptr ? pre_g[f] : bf2f(p.gnext[n]));
   for (int r = 0; r < rows; ++r) {
     const float x = ts[r * kTsLd + f];
     const size_t m = static_cast<size_t>(m0 + r);
     p.resid[m * p.ld_resid + n] = x;
     if (p.xg_out != nullptr) {
-      const float xg = x * bf2f(p.gnext[n]);
+      const float xg = x * gn;
       const uint16_t hi = f2bf(xg);
       p.xg_out[m * p.ld_xg + n] = hi;
       if (p.xg_lo != nullptr) p.xg_lo[m * p.ld_xg + n] = bf16_lo_part(xg, hi);
@@ -217,10 +224,47 @@ __device__ void epi_argmax(const GemmParams& p, const float* ts, int tile, int m
   }
 }
 
-// route: int scratch of 3 * route_cap entries (route_cap >= rows)
+// Routing of activation row m of the QKV epilogue: (request, position,
+// physical page), page -1 for block rows, -2 for a skipped or invalid
+// context row (an invalid page id also raises DFLASH_ERR_CAPACITY).
+__device__ __forceinline__ void qkv_route(const GemmParams& p, int m, int* req_out, int* pos_out,
+                                          int* pg_out) {
+  const QkvEpi& e = p.qkv;
+  int req, pos, pg = -1;
+  if (m < e.n_blk) {
+    req = m / e.block;
+    pos = e.anchor_pos[req] + m % e.block;
+  } else {
+    const int j = m - e.n_blk;
+    if (e.pool_req != nullptr) {
+      req = e.pool_req[j];
+      pos = e.pool_pos[j];
+    } else {
+      req = j / e.rows_per_req;
+      pos = e.pool_pos0[req] + j % e.rows_per_req;
+    }
+    if (pos < 0) {
+      pg = -2;
+    } else {
+      const int pi = pos / e.page_size;
+      pg = pi < e.max_pages ? e.page_table[static_cast<size_t>(req) * e.max_pages + pi] : -3;
+      if (pg < 0 || pg >= e.n_pages) {
+        raise_status(p.status, DFLASH_ERR_CAPACITY, 101);
+        pg = -2;
+      }
+    }
+  }
+  *req_out = req;
+  *pos_out = pos;
+  *pg_out = pg;
+}
+
+// route: int scratch of 3 * route_cap entries (route_cap >= rows); pre_route
+// (nullable): the routing of rows m0.. already computed, with stride pre_cap
 template <typename Sync>
 __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, int rows,
-                        int* route, int route_cap, int tid, Sync sync) {
+                        int* route, int route_cap, int tid, Sync sync,
+                        const int* pre_route = nullptr, int pre_cap = 0) {
     const QkvEpi& e = p.qkv;
   const int warp = tid / 32, lane = tid % 32;
   const int d = e.head_dim;
@@ -229,38 +273,16 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
   const int hq = e.n_q_heads, hkv = e.n_kv_heads;
   // Per-row routing, one thread per row, all lookups issued in parallel:
   // route[r] = (request, position, physical page or -1 for block rows / -2 skip)
-  int* r_req = route;
-  int* r_pos = route + route_cap;
-  int* r_pg = route + 2 * route_cap;
-  for (int r = tid; r < rows; r += 128) {
-    const int m = m0 + r;
-    int req, pos, pg = -1;
-    if (m < e.n_blk) {
-      req = m / e.block;
-      pos = e.anchor_pos[req] + m % e.block;
-    } else {
-      const int j = m - e.n_blk;
-      if (e.pool_req != nullptr) {
-        req = e.pool_req[j];
-        pos = e.pool_pos[j];
-      } else {
-        req = j / e.rows_per_req;
-        pos = e.pool_pos0[req] + j % e.rows_per_req;
-      }
-      if (pos < 0) {
-        pg = -2;
-      } else {
-        const int pi = pos / e.page_size;
-        pg = pi < e.max_pages ? e.page_table[static_cast<size_t>(req) * e.max_pages + pi] : -3;
-        if (pg < 0 || pg >= e.n_pages) {
-          raise_status(p.status, DFLASH_ERR_CAPACITY, 101);
-          pg = -2;
-        }
-      }
-    }
-    r_req[r] = req;
-    r_pos[r] = pos;
-    r_pg[r] = pg;
+  const int* r_req = route;
+  const int* r_pos = route + route_cap;
+  const int* r_pg = route + 2 * route_cap;
+  if (pre_route != nullptr) {
+    r_req = pre_route;
+    r_pos = pre_route + pre_cap;
+    r_pg = pre_route + 2 * pre_cap;
+  } else {
+    for (int r = tid; r < rows; r += 128)
+      qkv_route(p, m0 + r, route + r, route + route_cap + r, route + 2 * route_cap + r);
   }
   // Each (row, head) item is handled by a group of 8 lanes, 4 items per warp
   // at a time: lane `sub` of the group owns the rotate-half pairs

@@ -50,7 +50,16 @@ struct GemmCfg {
   static constexpr int SCRATCH_OFF = (TILE_BYTES + 255) / 256 * 256;
   static constexpr int RECV_OFF = SCRATCH_OFF;
   static_assert(SCRATCH_OFF + 4 * BN * 4 <= MAIN_BYTES, "epilogue scratch must fit the pipeline region");
-  static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + 1024;  // + barriers, alignment slack
+  // Epilogue inputs loaded during the main loop (decode-sized tiles only):
+  // row scales [32] and QKV routing [3][32]; the two-term BN = 16 variant
+  // (O projection and down: residual epilogue) also residual rows [4][128]
+  // and the next norm's gains [128].
+  static constexpr bool PRE = BN <= 32;
+  static constexpr bool PRE_RESID = PRE && SPLIT && BN == 16;
+  static constexpr int PRE_OFF = MAIN_BYTES + 256;
+  static constexpr int PRE_BYTES = !PRE ? 0 : (PRE_RESID ? 3072 : 512);
+  static constexpr int PRE_RESID_ROWS = 4;
+  static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + PRE_BYTES + 1024;  // + barriers, alignment slack
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
 };
 
@@ -172,6 +181,81 @@ __global__ void __launch_bounds__(128, 1)
   }
   if (!(warp == 0 && lane == 0)) griddep_wait();
   __syncwarp();
+
+  // ---------------- epilogue inputs, loaded by warps 2-3 (idle in the main
+  // loop) once the previous kernels' writes are visible, so that the tail
+  // after the last MMA starts with them in shared memory.  Same values and
+  // the same arithmetic as the epilogue's own loads.
+  float* pre_rinv = reinterpret_cast<float*>(smem + C::PRE_OFF);         // [32]
+  int* pre_route = reinterpret_cast<int*>(smem + C::PRE_OFF + 128);      // [3][32]
+  float* pre_resid = reinterpret_cast<float*>(smem + C::PRE_OFF + 512);  // [4][128]
+  float* pre_g = pre_resid + C::PRE_RESID_ROWS * kTileN;                 // [128]
+  const int rows_mt = min(BN, p.M - blockIdx.z * BN);                    // rows of this m-tile
+  bool have_rinv = false, have_route = false, have_resid = false;
+  if constexpr (C::PRE) {
+    have_rinv = p.ssq_in != nullptr;
+    have_route = p.mode == EPI_QKV;
+    if constexpr (C::PRE_RESID) {
+      // the rows this CTA will finish (as decided below): all of them, or
+      // its share of a split-K cluster
+      int rb = 0, rc = rows_mt;
+      if (p.splits > 1) {
+        if (p.cluster) {
+          int rpc = (rows_mt + p.splits - 1) / p.splits;
+          if (p.conv != nullptr && p.conv_width > 0) rpc = (rpc + p.block - 1) / p.block * p.block;
+          rb = min(rows_mt, static_cast<int>(cluster_ctarank()) * rpc);
+          rc = min(rows_mt, rb + rpc) - rb;
+        } else {
+          rc = C::PRE_RESID_ROWS + 1;  // the finishing CTA is known only at the end
+        }
+      }
+      have_resid = p.mode == EPI_RESID && rc <= C::PRE_RESID_ROWS;
+      if (have_resid && warp >= 2) {
+        const int t = tid - 64;
+        const int n0 = blockIdx.x * kTileN;
+        for (int idx = t; idx < rc * (kTileN / 4); idx += 64) {
+          const int r = idx / (kTileN / 4), c4 = idx % (kTileN / 4);
+          *reinterpret_cast<float4*>(pre_resid + r * kTileN + c4 * 4) = __ldcg(
+              reinterpret_cast<const float4*>(p.resid + static_cast<size_t>(blockIdx.z * BN + rb + r) * p.ld_resid + n0) + c4);
+        }
+        if (p.gnext != nullptr)
+          for (int f = t; f < kTileN; f += 64) pre_g[f] = bf2f(p.gnext[n0 + f]);
+      }
+    }
+    if (warp >= 2) {
+      const int w2 = warp - 2;
+      const int mt0 = blockIdx.z * BN;
+      if (have_rinv) {
+        // row r's sum: lane t adds tiles t, t+32, ... in order, then the xor
+        // butterfly of warp_sum (as in the epilogue below); rows w2, w2+2, ...
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+        for (int tt = lane; tt < p.ssq_in_tiles; tt += 32) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int r = w2 + 2 * i;
+            if (r < rows_mt) acc[i] += __ldcg(p.ssq_in + static_cast<size_t>(mt0 + r) * p.ssq_in_tiles + tt);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = w2 + 2 * i;
+          if (r < rows_mt) {
+            const float ss = warp_sum(acc[i]);
+            if (lane == 0)
+              pre_rinv[r] = (mt0 + r < p.norm_rows)
+                                ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps)
+                                : 1.f;
+          }
+        }
+      }
+      if (have_route) {
+        const int t = tid - 64;
+        if (t < rows_mt) qkv_route(p, mt0 + t, pre_route + t, pre_route + 32 + t, pre_route + 64 + t);
+      }
+    }
+  }
 
   // ---------------- epilogue: TMEM -> (partials | staged tile)
   const bool ok = mbar_wait(done, 0, abort_flag);
@@ -377,7 +461,9 @@ __global__ void __launch_bounds__(128, 1)
     // rows: one thread per row computes the same sums with all of the row's
     // loads in flight (a warp per row would wait one load round trip per row).
     float* rinv = reinterpret_cast<float*>(smem + C::SCRATCH_OFF);
-    if (rows_v <= 32) {
+    if (have_rinv) {
+      rinv = pre_rinv + r_beg;  // computed during the main loop
+    } else if (rows_v <= 32) {
       for (int r = warp; r < rows_v; r += 4) {
         const float* q = p.ssq_in + static_cast<size_t>(m0v + r) * p.ssq_in_tiles;
         float ss = 0.f;
@@ -416,12 +502,15 @@ __global__ void __launch_bounds__(128, 1)
     switch (p.mode) {
       case EPI_STORE_BF16:
       case EPI_STORE_F32: epi_store(p, tsv, tile, m0v, rows_v, tid, sync); break;
-      case EPI_RESID: epi_resid(p, tsv, tile, m0v, rows_v, tid, sync); break;
+      case EPI_RESID:
+        epi_resid(p, tsv, tile, m0v, rows_v, tid, sync, have_resid ? pre_resid : nullptr,
+                  have_resid && p.gnext != nullptr ? pre_g : nullptr);
+        break;
       case EPI_SWIGLU: epi_swiglu(p, tsv, tile, m0v, rows_v, tid, sync); break;
       case EPI_ARGMAX: epi_argmax(p, tsv, tile, m0v, rows_v, tid, sync, gridDim.x); break;
       case EPI_QKV:
         epi_qkv(p, tsv, tile, m0v, rows_v, reinterpret_cast<int*>(smem + C::SCRATCH_OFF + BN * 4), BN,
-                tid, sync);
+                tid, sync, have_route ? pre_route + r_beg : nullptr, 32);
         break;
       default: break;
     }

@@ -174,46 +174,12 @@ size_t attention_part_floats(int n_splits, int rows, int hq, int d);
 bool attention_cluster_ok(int d, int hq, int hkv, int n_splits);
 constexpr int kMaxAttnCluster = 16;
 
-// Persistent layer-stack kernel (persistent_stack.cu): the drafter stack and
-// LM head for block rows + context rows <= 32, one CTA per SM.
-struct PersistParams {
-  CUtensorMap m_wqkv, m_wo, m_gu, m_down, m_lm;  // weights (box 64 rows x 64)
-  CUtensorMap x_a, x_o, x_a2, x_h;               // activations (box 32 rows x 64)
-  GemmParams ep;     // epilogue template: pointers and strides shared by all phases
-  AttnParams att;    // attention template (pool patched per layer)
-  int n_layers, H, F, V, q_dim, kv_dim, qkv_rows, head_dim, nb, M_qkv, block, conv_width;
-  float eps;
-  const uint16_t* in_norm;
-  const uint16_t* post_norm;
-  const uint16_t* final_norm;
-  const uint16_t* conv;
-  uint16_t* pool;
-  size_t pool_layer_elems;
-  float* part;       // stream-K partial tiles
-  float* x;
-  uint16_t* a;
-  uint16_t* a2;
-  uint16_t* hmid;
-  float* ssq_a;
-  float* ssq_a2;
-  float* amax_val;
-  int32_t* amax_idx;
-  int32_t* draft;
-  float* logits;
-  unsigned* bar;     // grid-barrier counter, zeroed before the launch
-  int32_t* status;
-};
-int persistent_smem_bytes();
-int persistent_ctas(const PersistParams& p, int sms);
-size_t persistent_part_floats(const PersistParams& p, int n_ctas);
-cudaError_t persistent_launch(const PersistParams& p, int n_ctas, cudaStream_t s);
-
 // small kernels (small_kernels.cu)
 cudaError_t embed_block_launch(const int32_t* anchor, int batch, int block, const uint16_t* embed,
                                const uint16_t* mask_embed, const uint16_t* norm, int hidden,
                                float* x, uint16_t* a, int ld_a, float* ssq,
                                const uint16_t* pending, int T, cudaStream_t s, bool pdl,
-                               int32_t* status, int vocab, unsigned* zero_word = nullptr);
+                               int32_t* status, int vocab);
 cudaError_t embed_tokens_launch(const int32_t* tokens, int rows, const uint16_t* embed,
                                 const uint16_t* norm, int hidden, float* x, uint16_t* a,
                                 float* ssq, cudaStream_t s, bool pdl, int32_t* status,

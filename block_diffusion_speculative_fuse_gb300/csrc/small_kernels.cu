@@ -54,24 +54,48 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 // Per-row prologue of a layer stack: x[r] = float(src row), xg[r] =
 // bf16(x[r] * g) and ssq[r][t] = sum of x^2 over the 128-column tile t (the
-// next GEMM applies 1/rms per row).
+// next GEMM applies 1/rms per row).  Each thread takes 8 consecutive columns
+// (one 16-byte load of src and of g, all issued before any is used); the 16
+// threads of a tile sum their squares in a fixed order (per thread in column
+// order, then a 4-step xor butterfly over the 16 lanes).
 __device__ __forceinline__ void row_prologue(const uint16_t* src, const uint16_t* g, int H,
                                              float* x, uint16_t* xg, float* ssq) {
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = bf2f(src[c]);
-    x[c] = v;
-    xg[c] = f2bf(v * bf2f(g[c]));
-  }
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
-  for (int t = warp; t < H / 128; t += nw) {
-    float ss = 0.f;
+  constexpr int kMaxChunks = 4;  // H <= 8 * kRowThreads * kMaxChunks
+  uint4 sv[kMaxChunks], gv[kMaxChunks];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float v = bf2f(src[t * 128 + lane + 32 * k]);
-      ss = fmaf(v, v, ss);
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int c = (threadIdx.x + k * blockDim.x) * 8;
+    if (c < H) {
+      sv[k] = __ldg(reinterpret_cast<const uint4*>(src + c));
+      gv[k] = __ldg(reinterpret_cast<const uint4*>(g + c));
     }
-    ss = warp_sum(ss);
-    if (lane == 0) ssq[t] = ss;
+  }
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int c = (threadIdx.x + k * blockDim.x) * 8;
+    float ss = 0.f;
+    if (c < H) {
+      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(&sv[k]);
+      const uint16_t* g16 = reinterpret_cast<const uint16_t*>(&gv[k]);
+      float v[8];
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[j] = bf2f(s16[j]);
+        ss = fmaf(v[j], v[j], ss);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[j] = static_cast<uint32_t>(f2bf(v[2 * j] * bf2f(g16[2 * j]))) |
+               (static_cast<uint32_t>(f2bf(v[2 * j + 1] * bf2f(g16[2 * j + 1]))) << 16);
+      *reinterpret_cast<float4*>(x + c) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(x + c + 4) = make_float4(v[4], v[5], v[6], v[7]);
+      *reinterpret_cast<uint4*>(xg + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    // the 16 threads of a 128-column tile are 16 consecutive lanes
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, w);
+    if (c < H && (threadIdx.x % 16) == 0) ssq[c / 128] = ss;
   }
 }
 
@@ -82,15 +106,24 @@ __global__ void __launch_bounds__(kRowThreads)
     embed_block_kernel(const int32_t* anchor, int block, int n_blk, const uint16_t* embed,
                        const uint16_t* mask_embed, const uint16_t* g, int H, float* x,
                        uint16_t* a, int ld_a, float* ssq, const uint16_t* pending,
-                       int32_t* status, int vocab, unsigned* zero_word) {
+                       int32_t* status, int vocab) {
   griddep_launch_dependents();
   griddep_wait();
   const int r = blockIdx.x;
-  if (zero_word != nullptr && r == 0 && threadIdx.x == 0) *zero_word = 0u;
   if (r >= n_blk) {
-    const uint16_t* src = pending + static_cast<size_t>(r - n_blk) * H;
-    uint16_t* dst = a + static_cast<size_t>(r) * ld_a;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) dst[i] = src[i];
+    const uint4* src = reinterpret_cast<const uint4*>(pending + static_cast<size_t>(r - n_blk) * H);
+    uint4* dst = reinterpret_cast<uint4*>(a + static_cast<size_t>(r) * ld_a);
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
+      if (i < H / 8) v[k] = __ldcg(src + i);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
+      if (i < H / 8) dst[i] = v[k];
+    }
     return;
   }
   const int req = r / block, i = r % block;
@@ -128,19 +161,63 @@ __global__ void __launch_bounds__(kRowThreads)
                    uint16_t* raw_out, int ld_raw) {
   __shared__ float red[32];
   griddep_launch_dependents();
+  // the gains are not written by any kernel: load them before the wait
+  constexpr int kMaxChunks = 4;  // H <= 8 * kRowThreads * kMaxChunks
+  uint4 gv[kMaxChunks];
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int c = (threadIdx.x + k * blockDim.x) * 8;
+    if (c < H) gv[k] = __ldg(reinterpret_cast<const uint4*>(g + c));
+  }
   griddep_wait();
   const int r = blockIdx.x;
   const float* xr = x + static_cast<size_t>(r) * H;
+  // thread t takes columns 8t..8t+7 (+ 8 blockDim for the next chunk): every
+  // load in flight at once
+  float4 xv[kMaxChunks][2];
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int c = (threadIdx.x + k * blockDim.x) * 8;
+    if (c < H) {
+      xv[k][0] = __ldcg(reinterpret_cast<const float4*>(xr + c));
+      xv[k][1] = __ldcg(reinterpret_cast<const float4*>(xr + c + 4));
+    }
+  }
   float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = xr[c];
-    ss += v * v;
-    if (raw_out != nullptr) raw_out[static_cast<size_t>(r) * ld_raw + c] = f2bf(v);
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int c = (threadIdx.x + k * blockDim.x) * 8;
+    if (c < H) {
+      const float v[8] = {xv[k][0].x, xv[k][0].y, xv[k][0].z, xv[k][0].w,
+                          xv[k][1].x, xv[k][1].y, xv[k][1].z, xv[k][1].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
+      if (raw_out != nullptr) {
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = pack_bf2(v[2 * j], v[2 * j + 1]);
+        *reinterpret_cast<uint4*>(raw_out + static_cast<size_t>(r) * ld_raw + c) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
-  for (int c = threadIdx.x; c < H; c += blockDim.x)
-    out[static_cast<size_t>(r) * ld_out + c] = f2bf(xr[c] * inv * bf2f(g[c]));
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int c = (threadIdx.x + k * blockDim.x) * 8;
+    if (c < H) {
+      const float v[8] = {xv[k][0].x, xv[k][0].y, xv[k][0].z, xv[k][0].w,
+                          xv[k][1].x, xv[k][1].y, xv[k][1].z, xv[k][1].w};
+      const uint16_t* g16 = reinterpret_cast<const uint16_t*>(&gv[k]);
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[j] = pack_bf2(v[2 * j] * inv * bf2f(g16[2 * j]), v[2 * j + 1] * inv * bf2f(g16[2 * j + 1]));
+      *reinterpret_cast<uint4*>(out + static_cast<size_t>(r) * ld_out + c) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
 }
 
 // One warp per row: (max, lowest index) over the per-tile partials.
@@ -264,11 +341,10 @@ cudaError_t embed_block_launch(const int32_t* anchor, int batch, int block, cons
                                const uint16_t* mask_embed, const uint16_t* norm, int hidden,
                                float* x, uint16_t* a, int ld_a, float* ssq,
                                const uint16_t* pending, int T, cudaStream_t s, bool pdl,
-                               int32_t* status, int vocab, unsigned* zero_word) {
+                               int32_t* status, int vocab) {
   const int nb = batch * block;
   return launch(embed_block_kernel, dim3(nb + T), dim3(kRowThreads), 0, s, pdl, anchor, block, nb,
-                embed, mask_embed, norm, hidden, x, a, ld_a, ssq, pending, status, vocab,
-                zero_word);
+                embed, mask_embed, norm, hidden, x, a, ld_a, ssq, pending, status, vocab);
 }
 cudaError_t embed_tokens_launch(const int32_t* tokens, int rows, const uint16_t* embed,
                                 const uint16_t* norm, int hidden, float* x, uint16_t* a,

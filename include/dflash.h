@@ -70,7 +70,7 @@ extern "C" {
 typedef struct dflash_model_s* dflash_model;
 
 /* Shape of a decoder-layer stack: the drafter, or (for the end-to-end loop)
- * the target.  Supported: hidden % 128 == 0, head_dim in {64, 128},
+ * the target.  Supported: hidden % 128 == 0, hidden <= 8192, head_dim in {64, 128},
  * n_q_heads % n_kv_heads == 0 with group n_q_heads/n_kv_heads in {1,2,4,8},
  * (n_q_heads + 2 n_kv_heads) * head_dim % 128 == 0, mlp % 64 == 0,
  * vocab % 128 == 0, block in 1..32 (drafter), conv_width in {0,1,3,5,7},
