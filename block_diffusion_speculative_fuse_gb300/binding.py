@@ -32,7 +32,7 @@ class DflashConfig(ctypes.Structure):
                 ("n_taps", ctypes.c_int32), ("conv_width", ctypes.c_int32),
                 ("qk_norm", ctypes.c_int32), ("fc_norm", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("rms_eps", ctypes.c_float),
-                ("rope_base", ctypes.c_float)]
+                ("rope_base", ctypes.c_float), ("kv_terms", ctypes.c_int32)]
 
 
 WEIGHT_FIELDS = ["embed", "lm_head", "final_norm", "in_norm", "wqkv", "q_norm",
@@ -46,7 +46,8 @@ class DflashWeights(ctypes.Structure):
 
 class DflashKV(ctypes.Structure):
     _fields_ = [("pool", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
-                ("n_pages", ctypes.c_int32), ("max_pages", ctypes.c_int32)]
+                ("n_pages", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("n_rows", ctypes.c_int32)]
 
 
 EXPORTS = {

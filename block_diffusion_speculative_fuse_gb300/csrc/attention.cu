@@ -27,7 +27,7 @@ namespace dflash {
 
 constexpr int kAttnBufs = 2;  // double-buffered 64-key chunks (measured best)
 
-template <int D, int NW>
+template <int D, int NW, int TERMS>
 __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(128) uint8_t sm[];
   const int G = p.hq / p.hkv;
@@ -39,7 +39,8 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ A
   griddep_launch_dependents();
   griddep_wait();
   AttnAcc<D> acc;
-  if (!attn_accumulate<D, NW, kAttnBufs>(p, split, qt, req, g, tid, sm, CtaSync{}, acc)) return;
+  if (!attn_accumulate<D, NW, kAttnBufs, CtaSync, TERMS>(p, split, qt, req, g, tid, sm, CtaSync{}, acc))
+    return;
   const float (&o)[D / 8][4] = acc.o;
   const float* m_r = acc.m;
   const float* l_r = acc.l;
@@ -137,20 +138,20 @@ size_t attention_part_floats(int n_splits, int rows, int hq, int d) {
   return static_cast<size_t>(n_splits) * rows * hq * (d + 2);
 }
 
-template <int D, int NW>
+template <int D, int NW, int TERMS>
 static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
   static thread_local int attr_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, NW>,
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, NW, TERMS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         attn_smem_bytes<D, kAttnBufs>());
+                                         attn_smem_bytes<D, kAttnBufs, TERMS>());
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_kernel<D, NW>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(attn_kernel<D, NW, TERMS>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_kernel<D, NW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(attn_kernel<D, NW, TERMS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_device = dev;
   }
@@ -172,12 +173,12 @@ static cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_splits, (p.n + R - 1) / R, p.batch * p.hkv);
   cfg.blockDim = dim3(NW * 32, 1, 1);
-  cfg.dynamicSmemBytes = attn_smem_bytes<D, kAttnBufs>();
+  cfg.dynamicSmemBytes = attn_smem_bytes<D, kAttnBufs, TERMS>();
   cfg.stream = s;
   cfg.attrs = attrs;
   cfg.numAttrs = na;
   count_launch();
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_kernel<D, NW>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_kernel<D, NW, TERMS>, p);
   if (e != cudaSuccess || p.cluster) return e;
   cudaLaunchConfig_t c2 = {};
   const int vecs = p.batch * p.n * p.hq;
@@ -197,16 +198,21 @@ bool attention_cluster_ok(int d, int hq, int hkv, int n_splits) {
   return n_splits <= kMaxAttnCluster && (hq / hkv) <= 4 && (d == 64 || d == 128);
 }
 
-cudaError_t attention_launch(const AttnParams& p, cudaStream_t s, bool pdl) {
+template <int TERMS>
+static cudaError_t launch_terms(const AttnParams& p, cudaStream_t s, bool pdl) {
   const int G = p.hq / p.hkv;
   if (p.d == 128) {
-    if (G <= 4) return launch_attn<128, 4>(p, s, pdl);
-    if (G == 8) return launch_attn<128, 8>(p, s, pdl);
+    if (G <= 4) return launch_attn<128, 4, TERMS>(p, s, pdl);
+    if (G == 8) return launch_attn<128, 8, TERMS>(p, s, pdl);
   } else if (p.d == 64) {
-    if (G <= 4) return launch_attn<64, 4>(p, s, pdl);
-    if (G == 8) return launch_attn<64, 8>(p, s, pdl);
+    if (G <= 4) return launch_attn<64, 4, TERMS>(p, s, pdl);
+    if (G == 8) return launch_attn<64, 8, TERMS>(p, s, pdl);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t attention_launch(const AttnParams& p, cudaStream_t s, bool pdl) {
+  return p.kv_terms == 2 ? launch_terms<2>(p, s, pdl) : launch_terms<1>(p, s, pdl);
 }
 
 }  // namespace dflash

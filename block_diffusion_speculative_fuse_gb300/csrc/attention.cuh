@@ -44,14 +44,14 @@ constexpr int kChunk = 64;
 constexpr int kMaxSplitPages = 512;
 
 // K/V chunk buffers of the cp.async pipeline (NBUF-1 chunks in flight ahead
-// of the one being computed).
-template <int D, int NBUF>
+// of the one being computed); TERMS = 2 adds the low-term buffers of K and V.
+template <int D, int NBUF, int TERMS = 1>
 __host__ __device__ constexpr int attn_kv_bytes() {
-  return 2 /*K,V*/ * NBUF * kChunk * D * 2;
+  return 2 /*K,V*/ * TERMS * NBUF * kChunk * D * 2;
 }
-template <int D, int NBUF>
+template <int D, int NBUF, int TERMS = 1>
 __host__ __device__ constexpr int attn_smem_bytes() {
-  return attn_kv_bytes<D, NBUF>() + kMaxSplitPages * 4;
+  return attn_kv_bytes<D, NBUF, TERMS>() + kMaxSplitPages * 4;
 }
 
 // Byte offset of (key row, 16-byte column chunk) in a swizzled [64][D] tile.
@@ -71,12 +71,17 @@ struct AttnAcc {
 // over its key range, with NW warps (local thread index tid).  Leaves each
 // warp's unnormalised O and running (m, l) of its 16 query rows in acc.
 // Returns false when the query tile is past the request's rows.
-template <int D, int NW, int NBUF, typename Sync>
+// TERMS = 2: pool keys and values are hi + lo bf16 planes; S = Q K_hi^T +
+// Q K_lo^T and O += P V_hi + P V_lo accumulate both terms in fp32 (the
+// in-block keys of the drafter mode have one term: their lo tiles are zero).
+template <int D, int NW, int NBUF, typename Sync, int TERMS = 1>
 __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, int qt, int req,
                                                 int g, int tid, uint8_t* sm, Sync sync,
                                                 AttnAcc<D>& acc) {
   uint8_t* Kbuf = sm;
   uint8_t* Vbuf = sm + NBUF * kChunk * D * 2;
+  uint8_t* Klo = sm + 2 * NBUF * kChunk * D * 2;  // TERMS = 2 only
+  uint8_t* Vlo = sm + 3 * NBUF * kChunk * D * 2;
 
   const int G = p.hq / p.hkv;
   const int R = 16 * NW / G;  // query rows per CTA
@@ -131,7 +136,7 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
 
   const size_t plane = static_cast<size_t>(p.hkv) * p.page_size * D;  // K->V plane distance
   // stage this split's page ids (context keys only)
-  int* pages_s = reinterpret_cast<int*>(sm + attn_kv_bytes<D, NBUF>());
+  int* pages_s = reinterpret_cast<int*>(sm + attn_kv_bytes<D, NBUF, TERMS>());
   const int page_lo = k_lo / p.page_size;
   if (!blk && k_hi > k_lo) {
     const int npg = (k_hi - 1) / p.page_size + 1 - page_lo;  // <= kMaxSplitPages (host caps S)
@@ -153,7 +158,7 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
       const int key = kc + kr;
       const uint16_t* sk = p.q;  // any valid address for a zero-fill copy
       const uint16_t* sv = p.q;
-      int bytes = 0;
+      int bytes = 0, bytes_lo = 0;
       if (key < k_hi) {
         if (blk) {
           const size_t o = ((static_cast<size_t>(req) * p.hkv + g) * p.n + key) * D + ch * 8;
@@ -163,17 +168,22 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
         } else {
           const int pg = pages_s[key / p.page_size - page_lo];
           if (pg >= 0) {
-            const size_t o = (static_cast<size_t>(pg) * 2 * p.hkv + g) * p.page_size * D +
+            const size_t o = (static_cast<size_t>(pg) * 2 * TERMS * p.hkv + g) * p.page_size * D +
                              static_cast<size_t>(key % p.page_size) * D + ch * 8;
             sk = p.pool + o;
             sv = p.pool + o + plane;
             bytes = 16;
+            bytes_lo = 16;
           }
         }
       }
       const uint32_t off = buf * kChunk * D * 2 + swz<D>(kr, ch);
       cp_async16(Kbuf + off, sk, bytes);
       cp_async16(Vbuf + off, sv, bytes);
+      if constexpr (TERMS == 2) {
+        cp_async16(Klo + off, bytes_lo ? sk + 2 * plane : p.q, bytes_lo);
+        cp_async16(Vlo + off, bytes_lo ? sv + 2 * plane : p.q, bytes_lo);
+      }
     }
     cp_async_commit();
   };
@@ -228,6 +238,17 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
       for (int j = 0; j < 8; ++j) mma16816(s[j], qf[kk], bb[j][0], bb[j][1]);
 #pragma unroll
       for (int j = 0; j < 8; ++j) mma16816(s[j], qf[kk + 1], bb[j][2], bb[j][3]);
+      if constexpr (TERMS == 2) {
+        const uint32_t klo = smem_u32(Klo) + buf * kChunk * D * 2;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          ldsm_x4(klo + swz<D>(j * 8 + (lane & 7), kk * 2 + (lane >> 3)), bb[j][0], bb[j][1],
+                  bb[j][2], bb[j][3]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mma16816(s[j], qf[kk], bb[j][0], bb[j][1]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mma16816(s[j], qf[kk + 1], bb[j][2], bb[j][3]);
+      }
     }
     // mask + scale (log2 domain)
 #pragma unroll
@@ -285,6 +306,12 @@ __device__ __forceinline__ bool attn_accumulate(const AttnParams& p, int split, 
         ldsm_x4_t(vbase + swz<D>(krow, nd + (lane >> 4)), b0, b1, b2, b3);
         mma16816(o[nd], a, b0, b1);
         mma16816(o[nd + 1], a, b2, b3);
+        if constexpr (TERMS == 2) {
+          const uint32_t vlo = smem_u32(Vlo) + buf * kChunk * D * 2;
+          ldsm_x4_t(vlo + swz<D>(krow, nd + (lane >> 4)), b0, b1, b2, b3);
+          mma16816(o[nd], a, b0, b1);
+          mma16816(o[nd + 1], a, b2, b3);
+        }
       }
     }
     sync();

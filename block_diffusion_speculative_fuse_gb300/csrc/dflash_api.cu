@@ -291,9 +291,11 @@ QkvEpi qkv_base(const dflash_model_s* m, int layer) {
   return e;
 }
 
+int kv_terms_of(const dflash_config& c) { return c.kv_terms == 2 ? 2 : 1; }
+
 size_t layer_pool_elems(const dflash_model_s* m, const dflash_kv* kv) {
-  return static_cast<size_t>(kv->n_pages) * 2 * m->cfg.n_kv_heads * m->cfg.page_size *
-         m->cfg.head_dim;
+  return static_cast<size_t>(kv->n_pages) * 2 * kv_terms_of(m->cfg) * m->cfg.n_kv_heads *
+         m->cfg.page_size * m->cfg.head_dim;
 }
 
 void set_pool(const dflash_model_s* m, QkvEpi& e, const dflash_kv* kv, int layer) {
@@ -301,11 +303,13 @@ void set_pool(const dflash_model_s* m, QkvEpi& e, const dflash_kv* kv, int layer
   e.page_table = kv->page_table;
   e.max_pages = kv->max_pages;
   e.n_pages = kv->n_pages;
+  e.n_req = kv->n_rows;
+  e.kv_terms = kv_terms_of(m->cfg);
 }
 
 int check_kv(const dflash_model_s* m, const dflash_kv* kv) {
   if (kv == nullptr || kv->pool == nullptr || kv->page_table == nullptr || kv->n_pages <= 0 ||
-      kv->max_pages <= 0)
+      kv->max_pages <= 0 || kv->n_rows <= 0)
     return DFLASH_ERR_INVALID_ARG;
   if (!aligned16(kv->pool)) return DFLASH_ERR_INVALID_ARG;
   (void)m;
@@ -426,6 +430,7 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       a.pos0 = pos0;
       a.causal = m->is_draft ? 0 : 1;
       a.pool = static_cast<const uint16_t*>(kv->pool) + layer_pool_elems(m, kv) * l;
+      a.kv_terms = kv_terms_of(c);
       a.page_table = kv->page_table;
       a.max_pages = kv->max_pages;
       a.n_pages = kv->n_pages;
@@ -534,6 +539,7 @@ int check_cfg(const dflash_config* c, bool draft) {
   if (((c->n_q_heads + 2 * c->n_kv_heads) * c->head_dim) % 128) return DFLASH_ERR_UNSUPPORTED;
   if ((c->n_q_heads * c->head_dim) % 64 || c->mlp < 64 || c->mlp % 64) return DFLASH_ERR_UNSUPPORTED;
   if (c->page_size != 16) return DFLASH_ERR_UNSUPPORTED;
+  if (c->kv_terms < 0 || c->kv_terms > 2 || (draft && c->kv_terms == 2)) return DFLASH_ERR_UNSUPPORTED;
   if (draft) {
     if (c->block < 1 || c->block > 32 || 256 % c->block) return DFLASH_ERR_UNSUPPORTED;
     if (c->n_taps < 1) return DFLASH_ERR_UNSUPPORTED;
@@ -786,6 +792,7 @@ int dflash_draft_block(dflash_model m, const int32_t* anchor, const int32_t* anc
     return DFLASH_ERR_INVALID_ARG;
   int rc = check_kv(m, kv);
   if (rc) return rc;
+  if (batch > kv->n_rows) return DFLASH_ERR_CAPACITY;
   const dflash_config& c = m->cfg;
   const int B = c.block;
   const int rows = batch * B;
@@ -856,6 +863,7 @@ int dflash_target_forward(dflash_model m, const int32_t* tokens, const int32_t* 
     return DFLASH_ERR_INVALID_ARG;
   int rc = check_kv(m, kv);
   if (rc) return rc;
+  if (batch > kv->n_rows) return DFLASH_ERR_CAPACITY;
   const dflash_config& c = m->cfg;
   std::vector<int32_t> slot(c.n_layers, -1);
   for (int i = 0; i < n_taps; ++i) {

@@ -226,7 +226,8 @@ __device__ void epi_argmax(const GemmParams& p, const float* ts, int tile, int m
 
 // Routing of activation row m of the QKV epilogue: (request, position,
 // physical page), page -1 for block rows, -2 for a skipped or invalid
-// context row (an invalid page id also raises DFLASH_ERR_CAPACITY).
+// context row (an invalid request index or page id also raises
+// DFLASH_ERR_CAPACITY).
 __device__ __forceinline__ void qkv_route(const GemmParams& p, int m, int* req_out, int* pos_out,
                                           int* pg_out) {
   const QkvEpi& e = p.qkv;
@@ -243,7 +244,11 @@ __device__ __forceinline__ void qkv_route(const GemmParams& p, int m, int* req_o
       req = j / e.rows_per_req;
       pos = e.pool_pos0[req] + j % e.rows_per_req;
     }
-    if (pos < 0) {
+    if (req < 0 || req >= e.n_req) {
+      if (pos >= 0) raise_status(p.status, DFLASH_ERR_CAPACITY, 102);
+      req = 0;
+      pg = -2;
+    } else if (pos < 0) {
       pg = -2;
     } else {
       const int pi = pos / e.page_size;
@@ -352,14 +357,18 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
     }
     if (!act) continue;
     uint16_t* dst;
+    uint16_t* dst_lo = nullptr;  // low terms (two-term cache)
     if (kind == 0) {
       dst = e.q + (static_cast<size_t>(m) * hq + hidx) * d;
     } else if (is_blk) {
       dst = (kind == 1 ? e.kblk : e.vblk) +
             ((static_cast<size_t>(req) * hkv + hidx) * e.block + m % e.block) * d;
     } else {
-      dst = e.pool + ((((static_cast<size_t>(pg) * 2 + (kind - 1)) * hkv + hidx) * e.page_size) +
+      const int planes = 2 * e.kv_terms;
+      const size_t plane = static_cast<size_t>(hkv) * e.page_size * d;
+      dst = e.pool + ((((static_cast<size_t>(pg) * planes + (kind - 1)) * hkv + hidx) * e.page_size) +
                       pos % e.page_size) * d;
+      if (e.kv_terms == 2) dst_lo = dst + 2 * plane + c0;
     }
     dst += c0;
     uint32_t u1[4], u2[4];
@@ -374,6 +383,23 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
     } else {
       *reinterpret_cast<uint2*>(dst) = make_uint2(u1[0], u1[1]);
       *reinterpret_cast<uint2*>(dst + half) = make_uint2(u2[0], u2[1]);
+    }
+    if (dst_lo != nullptr) {
+      // v = hi + lo with lo = bf16(v - hi)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        u1[j] = pack_bf2(x1[2 * j] - bf2f(static_cast<uint16_t>(u1[j] & 0xFFFFu)),
+                         x1[2 * j + 1] - bf2f(static_cast<uint16_t>(u1[j] >> 16)));
+        u2[j] = pack_bf2(x2[2 * j] - bf2f(static_cast<uint16_t>(u2[j] & 0xFFFFu)),
+                         x2[2 * j + 1] - bf2f(static_cast<uint16_t>(u2[j] >> 16)));
+      }
+      if (P == 8) {
+        *reinterpret_cast<uint4*>(dst_lo) = make_uint4(u1[0], u1[1], u1[2], u1[3]);
+        *reinterpret_cast<uint4*>(dst_lo + half) = make_uint4(u2[0], u2[1], u2[2], u2[3]);
+      } else {
+        *reinterpret_cast<uint2*>(dst_lo) = make_uint2(u1[0], u1[1]);
+        *reinterpret_cast<uint2*>(dst_lo + half) = make_uint2(u2[0], u2[1]);
+      }
     }
   }
 }

@@ -51,6 +51,8 @@ struct QkvEpi {
   uint16_t* pool;        // layer base [n_pages][2][hkv][page][d]
   const int32_t* page_table;
   int max_pages, n_pages, page_size;
+  int n_req;             // rows of page_table: explicit pool_req values must lie in [0, n_req)
+  int kv_terms;          // 1: bf16 K/V planes; 2: also bf16 low terms (planes 2, 3)
   float2 rope[kMaxRopePairs];  // inv_freq of pair p as (hi, lo) float pair
 };
 
@@ -128,6 +130,7 @@ struct AttnParams {
   const uint16_t* pool;  // layer base
   const int32_t* page_table;
   int max_pages, n_pages, page_size;
+  int kv_terms;          // 2: K and V also have bf16 low-term planes (2, 3)
   const uint16_t* kblk;  // [batch][hkv][n][d] (non-causal)
   const uint16_t* vblk;
   int hq, hkv, d;

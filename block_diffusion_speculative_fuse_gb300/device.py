@@ -19,7 +19,8 @@ def make_config(shape, block=0, n_taps=0, conv_width=0, fc_norm=True, page_size=
         n_kv_heads=shape.n_kv_heads, head_dim=shape.head_dim, mlp=shape.mlp,
         vocab=shape.vocab, block=block, n_taps=n_taps, conv_width=conv_width,
         qk_norm=1 if shape.qk_norm else 0, fc_norm=1 if fc_norm else 0,
-        page_size=page_size, rms_eps=shape.rms_eps, rope_base=shape.rope_base)
+        page_size=page_size, rms_eps=shape.rms_eps, rope_base=shape.rope_base,
+        kv_terms=getattr(shape, "kv_terms", 1))
 
 
 class DeviceModel:
@@ -67,20 +68,23 @@ class DeviceModel:
 
 
 class PagedKV:
-    """A paged KV pool [L][n_pages][2][hkv][page][d] (bf16) and page table."""
+    """A paged KV pool [L][n_pages][2*kv_terms][hkv][page][d] (bf16) and page
+    table (planes K, V, then the low terms of K and V for a two-term cache)."""
 
     def __init__(self, shape, page_table: np.ndarray, n_pages: int, page_size=16,
                  device="cuda", zero=True):
         L, hkv, d = shape.n_layers, shape.n_kv_heads, shape.head_dim
+        planes = 2 * getattr(shape, "kv_terms", 1)
         alloc = torch.zeros if zero else torch.empty
-        self.pool = alloc((L, n_pages, 2, hkv, page_size, d), dtype=torch.bfloat16,
+        self.pool = alloc((L, n_pages, planes, hkv, page_size, d), dtype=torch.bfloat16,
                           device=device)
         self.table_np = np.ascontiguousarray(page_table, dtype=np.int32)
         self.table = torch.from_numpy(self.table_np).to(device)
         self.page_size = page_size
         self.n_pages = n_pages
         self.struct = B.DflashKV(pool=self.pool.data_ptr(), page_table=self.table.data_ptr(),
-                                 n_pages=n_pages, max_pages=self.table_np.shape[1])
+                                 n_pages=n_pages, max_pages=self.table_np.shape[1],
+                                 n_rows=self.table_np.shape[0])
 
     def fill_logical(self, layer: int, req: int, k_u16: np.ndarray, v_u16: np.ndarray):
         """Place already-projected context K/V ([len][hkv][d], bf16 bits) of

@@ -91,6 +91,12 @@ typedef struct {
   int32_t page_size;  /* KV page size in positions (16)                            */
   float rms_eps;
   float rope_base;
+  /* K/V cache terms: 1 = K and V in bf16; 2 = each stored as two bf16 planes
+   * hi = bf16(v), lo = bf16(v - hi) (about 16 significant bits; the attention
+   * multiplies both into one fp32 accumulator).  2 is for a target model only:
+   * its logits at 8 layers and H = 4096 stay within 0.05 of exact arithmetic
+   * only with the two-term cache.  0 is read as 1. */
+  int32_t kv_terms;
 } dflash_config;
 
 /* Device pointers, all bf16, stacked over layers where marked [L].
@@ -115,16 +121,22 @@ typedef struct {
 } dflash_weights;
 
 /* A paged KV cache (the drafter's context cache, or the target's cache).
- * pool: bf16 [n_layers][n_pages][2][n_kv_heads][page_size][head_dim]
- *       (plane 0 = K after k-norm and RoPE, plane 1 = V);
- * page_table: int32 [batch][max_pages], entry = physical page index.
+ * pool: bf16 [n_layers][n_pages][2*kv_terms][n_kv_heads][page_size][head_dim]
+ *       (plane 0 = K after k-norm and RoPE, plane 1 = V; with kv_terms = 2,
+ *       planes 2 and 3 hold the low terms of K and V);
+ * page_table: int32 [n_rows][max_pages], entry = physical page index; row r
+ * belongs to request r (n_rows = the requests the cache can hold).
  * Logical position p of request r lives in page page_table[r][p / page_size]
- * at slot p % page_size.  Pages may be in any physical order. */
+ * at slot p % page_size.  Pages may be in any physical order.  Request
+ * indices read from device arrays (row_req, pending_req) outside
+ * [0, n_rows), and page ids outside [0, n_pages), are recorded as
+ * DFLASH_ERR_CAPACITY in the workspace status word and the row is skipped. */
 typedef struct {
   void* pool;
   const int32_t* page_table;
   int32_t n_pages;
   int32_t max_pages;
+  int32_t n_rows;
 } dflash_kv;
 
 /* ------------------------------------------------------------------ model */
@@ -164,10 +176,9 @@ int dflash_ctx_fuse(dflash_model m, const void* taps, int32_t T, void* ctx, void
 /* For every layer l: K = RoPE(knorm(W_k^l c_t), pos_t), V = W_v^l c_t, stored
  * at logical position row_pos[t] of request row_req[t].  Rows with
  * row_pos[t] < 0 are skipped.  ctx: bf16 [T][hidden].  m must be a drafter
- * (DFLASH_ERR_INVALID_ARG for a target model).  row_req[t] must name a row
- * of kv->page_table (0 <= row_req[t] < its row count): dflash_kv carries no
- * row count, so the kernels check the page index and the page id they read
- * but cannot check the request index. */
+ * (DFLASH_ERR_INVALID_ARG for a target model).  A row_req[t] outside
+ * [0, kv->n_rows) is recorded as DFLASH_ERR_CAPACITY in the status word and
+ * its row is skipped. */
 int dflash_kv_append(dflash_model m, const void* ctx, const int32_t* row_req,
                      const int32_t* row_pos, int32_t T, const dflash_kv* kv, void* ws,
                      size_t ws_bytes, void* stream);
@@ -192,7 +203,8 @@ int dflash_kv_append(dflash_model m, const void* ctx, const int32_t* row_req,
 int dflash_ctx_fuse_noalloc(dflash_model m, const void* taps, int32_t T, void* ctx,
                             void* stream);
 
-/* One drafter pass for `batch` requests.  Request r's anchor token
+/* One drafter pass for `batch` requests (batch <= kv->n_rows, else
+ * DFLASH_ERR_CAPACITY before any launch).  Request r's anchor token
  * anchor[r] sits at position L_r = anchor_pos[r]; block position i at L_r+i;
  * block rows attend to context positions [0, L_r) of the cache and to all B
  * block positions.  If T > 0, the T pending context rows (pending_ctx bf16
@@ -232,7 +244,8 @@ int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t ba
 
 /* ----------------------------------------------- end-to-end loop helpers */
 
-/* Causal target forward over `batch` requests x `n` consecutive rows:
+/* Causal target forward over `batch` requests x `n` consecutive rows
+ * (batch <= kv->n_rows, else DFLASH_ERR_CAPACITY before any launch):
  * tokens int32 [batch][n], row i of request r at position pos0[r] + i.  Each
  * row's K/V are written to the target cache at its position, then each row
  * attends to positions [0, pos0[r] + i] of its request.  tap_layers is a

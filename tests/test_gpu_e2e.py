@@ -86,6 +86,37 @@ def test_tiny_e2e_spec_equals_ar_and_oracle():
     assert np.array_equal(ar[0][sure], np.argmax(lg, -1)[sure])
 
 
+def test_tiny_e2e_at_configured_init_spec_equals_ar_and_oracle():
+    """tiny_e2e with the target drawn from N(0, 0.02), as the workload states.
+    GPU speculative == GPU autoregressive for the whole run; against the
+    oracle under teacher forcing every logit is within 0.05 and the token
+    agrees wherever the oracle's top-1/top-2 gap exceeds 0.1 (at this init
+    the logits are small, so few positions have such a gap; the 0.05-std
+    test above checks the token rule on many more)."""
+    from block_diffusion_speculative_fuse_gb300.device import i32
+    from block_diffusion_speculative_fuse_gb300.generate import SpecDecoder, TargetRunner, \
+        ar_generate
+    wl = W.get_workload("tiny_e2e")
+    shared, tw, dw, tm, dm = models(wl, target_std=0.02)
+    P, N = wl.prompt_len, wl.gen_tokens
+    prompt = W.uniform_tokens(P, wl.target.vocab, wl.wid, W.TENSOR_IDS["prompt"])[None]
+    ar = ar_generate(TargetRunner(tm, 1, P + N + 1, P), prompt, N)
+    sd = SpecDecoder(tm, dm, wl.tap_layers, 1, P + N)
+    assert np.array_equal(sd.generate(prompt, N), ar)
+    seq = np.concatenate([prompt[0], ar[0, :-1]])
+    run = TargetRunner(tm, 1, len(seq) + 1, len(seq))
+    logits = torch.zeros((len(seq), wl.target.vocab), dtype=torch.float32, device="cuda")
+    run.forward(i32(seq[None]), i32([0]), len(seq), logits=logits)
+    torch.cuda.synchronize()
+    tws = O.LayerStack(wl.target, tw, shared)
+    lref, _ = O.target_rows(wl.target, tws, seq, 0, O.TargetCache(wl.target, len(seq) + 1))
+    assert np.abs(logits.cpu().numpy() - lref).max() <= 0.05
+    lg = lref[P - 1:]
+    top = np.sort(lg, axis=-1)
+    sure = (top[:, -1] - top[:, -2]) > 0.1
+    assert np.array_equal(ar[0][sure], np.argmax(lg, -1)[sure])
+
+
 @pytest.mark.parametrize("block", [1, 4])
 def test_spec_equals_ar_other_block_sizes(block):
     from dataclasses import replace

@@ -1,0 +1,93 @@
+"""The end-to-end workload's shapes on the GPU, shortened: the 8-layer
+H=4096 target (32 query / 8 KV heads, head_dim 128, SwiGLU 12288, vocab
+151936, N(0, 0.02) init) and the Qwen3-8B-shaped 5-layer B=16 drafter fed
+from target layers {1, 2, 4, 6, 7}; batch 2, prompts of 64 tokens, 48
+generated tokens (every iteration a block verify of 16 rows per request).
+
+Losslessness at these shapes: GPU speculative output == GPU autoregressive
+output for both requests ("DFlash: how block diffusion boosts NVIDIA
+Blackwell throughput", introduction: lossless; "NVIDIA tests DFlash to cut
+LLM inference bottlenecks", section "DFlash moves drafting to parallel
+compute": the target verifies the whole block in one parallel pass).  Against
+the oracle, request 0 under teacher forcing (its prompt and the first 16
+generated tokens): target logits within 0.05, tapped hidden states within
+2e-2 (row-norm relative), argmax equal wherever the oracle's top-1/top-2 gap
+exceeds 0.1.
+
+The fp64 oracle holds about 28 GB of decoded weights on the host; the test
+skips when the host has less than 96 GB available, rather than risk running
+the machine out of memory.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workload as W
+
+pytestmark = pytest.mark.gpu
+
+P, N, BATCH, ORACLE_EXTRA = 64, 48, 2, 16
+
+
+def mem_available_gb():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) / 1e6
+    except OSError:
+        pass
+    return 0.0
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_diffusion_speculative_fuse_gb300 import _build, binding
+    _build.build()
+    binding.load()
+
+
+def test_e2e_8layer_shapes_spec_equals_ar_and_oracle():
+    if mem_available_gb() < 96:
+        pytest.skip(f"host memory available {mem_available_gb():.0f} GB < 96 GB for the fp64 oracle")
+    from block_diffusion_speculative_fuse_gb300.device import DeviceModel, i32
+    from block_diffusion_speculative_fuse_gb300.generate import SpecDecoder, TargetRunner, \
+        ar_generate
+    wl = W.get_workload("e2e_8layer")
+    ts, ds = wl.target, wl.draft
+    V = ts.vocab
+    shared = W.shared_weights(ts, wl.wid)
+    tw = W.target_weights(ts, wl.wid)
+    tm = DeviceModel(ts, tw, shared, draft=False)
+    dm = DeviceModel(ds, W.draft_weights(ds, wl.wid), {k: tm.t[k] for k in ("embed", "lm_head")},
+                     draft=True)
+    prompts = W.uniform_tokens(BATCH * P, V, wl.wid, W.TENSOR_IDS["prompt"]).reshape(BATCH, P)
+    ar = ar_generate(TargetRunner(tm, BATCH, P + N + 1, P), prompts, N)
+    sd = SpecDecoder(tm, dm, wl.tap_layers, BATCH, P + N)
+    sp = sd.generate(prompts, N)
+    assert np.array_equal(sp, ar), "speculative output differs from autoregressive output"
+    assert all(0 <= n <= ds.block - 1 for n in sd.stats)
+    assert len(sd.stats) >= 3 * BATCH
+
+    # oracle, request 0, teacher forcing on the GPU's own tokens
+    seq = np.concatenate([prompts[0], ar[0, :ORACLE_EXTRA]])
+    run = TargetRunner(tm, 1, len(seq) + 1, len(seq), wl.tap_layers)
+    logits = torch.zeros((len(seq), V), dtype=torch.float32, device="cuda")
+    out, taps = run.forward(i32(seq[None]), i32([0]), len(seq), want_taps=True, logits=logits)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    hg = taps.float().cpu().numpy()
+    toks = out.cpu().numpy()[0]
+    del tm, dm
+    tws = O.LayerStack(ts, tw, shared)
+    lref, href = O.target_rows(ts, tws, seq, 0, O.TargetCache(ts, len(seq) + 1), wl.tap_layers)
+    err = np.abs(lg - lref).max()
+    assert err <= 0.05, f"max |dlogit| {err:.4f}"
+    rel = np.max(np.linalg.norm(hg - href, axis=1) / np.linalg.norm(href, axis=1))
+    assert rel <= 2e-2, f"tapped states rel err {rel:.4f}"
+    top = np.sort(lref, axis=-1)
+    sure = (top[:, -1] - top[:, -2]) > 0.1
+    assert sure.sum() > 0
+    assert np.array_equal(toks[sure], np.argmax(lref, -1)[sure])

@@ -114,6 +114,41 @@ def test_bad_page_id_reports_capacity_and_recovers(tc, monkeypatch):
     assert torch.equal(again, clean)
 
 
+def test_bad_request_index_reports_capacity_and_recovers():
+    """Pending context rows whose request index lies outside the page table
+    (one past its last row, and a negative one): the K/V routing records
+    DFLASH_ERR_CAPACITY at site 102 and skips those rows instead of reading
+    the page table out of bounds.  A batch larger than the table is refused
+    before any launch.  With the indices repaired and the status cleared, the
+    next step gives the clean step's logits bit for bit."""
+    from block_diffusion_speculative_fuse_gb300.session import DraftStep
+    wl = tiny_workload("badreq", wid=814, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                       mlp=256, vocab=1024, block=16, batch=3, ctx_len_range=(20, 300))
+    st = DraftStep(wl)
+    rows = st.batch * st.B
+    clean = torch.zeros((rows, wl.draft.vocab), dtype=torch.float32, device="cuda")
+    assert run_draft(st, clean) == (0, 0)
+    good = st.pending_req.clone()
+    st.pending_req[0] = st.kv.table.shape[0]
+    st.pending_req[-1] = -2
+    bad = torch.zeros_like(clean)
+    assert run_draft(st, bad) == (CAPACITY, 102)
+    st.pending_req.copy_(good)
+    B_().dflash_workspace_init(st.ws)
+    # more requests than the page table has rows: rejected on the host
+    B = B_()
+    big = torch.zeros(st.batch + 1, dtype=torch.int32, device="cuda")
+    draft = torch.zeros((st.batch + 1, st.B - 1), dtype=torch.int32, device="cuda")
+    with pytest.raises(B.DflashError) as e:
+        B.dflash_draft_block(st.model.handle, big, big, st.batch + 1, st.kv.struct, None, None,
+                             None, 0, draft, None, None, st.ws)
+    assert e.value.code == CAPACITY
+    assert B.dflash_get_status(st.ws) == (0, 0)
+    again = torch.zeros_like(clean)
+    assert run_draft(st, again) == (0, 0)
+    assert torch.equal(again, clean)
+
+
 # -------------------------------------------------------------- determinism
 @pytest.mark.parametrize("kw", [
     # long contexts: several key splits per request, merged in split order
