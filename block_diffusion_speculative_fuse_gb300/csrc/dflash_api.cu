@@ -79,6 +79,7 @@ struct dflash_model_s {
   // GEMM: k-blocks its producer still has to request when the next kernel
   // may launch (< 0: at the start)
   int dep_lead = 2;
+  int pre_mask = 15;  // GEMM epilogue inputs loaded during the main loop (GemmParams::pre_mask)
   CUtensorMap m_wqkv, m_wo, m_gu, m_down, m_lm, m_fc;
   float2 rope[kMaxRopePairs];
   int qkv_rows = 0, q_dim = 0, kv_dim = 0;
@@ -246,6 +247,7 @@ GemmParams gemm_base(const dflash_model_s* m, int M, int N, int K, int bn, Ws& w
   p.counters = ws.counters();
   p.status = ws.status();
   p.dep_lead = m->dep_lead;
+  p.pre_mask = m->pre_mask;
   return p;
 }
 
@@ -628,6 +630,8 @@ int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflas
     // has k weight k-blocks left to request (-1: at the start)
     const char* dl = std::getenv("DFLASH_DEP_LEAD");
     if (dl != nullptr && dl[0] != 0) m->dep_lead = std::atoi(dl);
+    const char* pm = std::getenv("DFLASH_PRE_MASK");
+    if (pm != nullptr && pm[0] != 0) m->pre_mask = std::atoi(pm);
   }
   if (draft && m->attn_tc && (cfg->head_dim == 64 || cfg->head_dim == 128))
     attention_tc_prepare(cfg->head_dim);

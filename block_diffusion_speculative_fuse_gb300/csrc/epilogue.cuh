@@ -265,11 +265,14 @@ __device__ __forceinline__ void qkv_route(const GemmParams& p, int m, int* req_o
 }
 
 // route: int scratch of 3 * route_cap entries (route_cap >= rows); pre_route
-// (nullable): the routing of rows m0.. already computed, with stride pre_cap
+// (nullable): the routing of rows m0.. already computed, with stride pre_cap;
+// pre_gain / pre_cs (nullable): the tile's q/k-norm gains [d] and the RoPE
+// (cos, sin) of rows m0.. [rows][64] already computed.
 template <typename Sync>
 __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, int rows,
                         int* route, int route_cap, int tid, Sync sync,
-                        const int* pre_route = nullptr, int pre_cap = 0) {
+                        const int* pre_route = nullptr, int pre_cap = 0,
+                        const float* pre_gain = nullptr, const float2* pre_cs = nullptr) {
     const QkvEpi& e = p.qkv;
   const int warp = tid / 32, lane = tid % 32;
   const int d = e.head_dim;
@@ -298,14 +301,16 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
   const int c0 = sub * P;
   float gq1[8], gq2[8], gk1[8], gk2[8];
   float2 rf[8];
+  if (pre_gain == nullptr) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const bool in = j < P;
-    gq1[j] = (in && e.q_norm != nullptr) ? bf2f(e.q_norm[c0 + j]) : 1.f;
-    gq2[j] = (in && e.q_norm != nullptr) ? bf2f(e.q_norm[half + c0 + j]) : 1.f;
-    gk1[j] = (in && e.k_norm != nullptr) ? bf2f(e.k_norm[c0 + j]) : 1.f;
-    gk2[j] = (in && e.k_norm != nullptr) ? bf2f(e.k_norm[half + c0 + j]) : 1.f;
-    rf[j] = in ? e.rope[c0 + j] : make_float2(0.f, 0.f);
+    for (int j = 0; j < 8; ++j) {
+      const bool in = j < P;
+      gq1[j] = (in && e.q_norm != nullptr) ? bf2f(e.q_norm[c0 + j]) : 1.f;
+      gq2[j] = (in && e.q_norm != nullptr) ? bf2f(e.q_norm[half + c0 + j]) : 1.f;
+      gk1[j] = (in && e.k_norm != nullptr) ? bf2f(e.k_norm[c0 + j]) : 1.f;
+      gk2[j] = (in && e.k_norm != nullptr) ? bf2f(e.k_norm[half + c0 + j]) : 1.f;
+      rf[j] = in ? e.rope[c0 + j] : make_float2(0.f, 0.f);
+    }
   }
   sync();
   const int items = rows * per_tile;
@@ -343,15 +348,29 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
     if (kind < 2) {
       const bool norm = kind == 0 ? (e.q_norm != nullptr) : (e.k_norm != nullptr);
       const float inv = norm ? rsqrtf(ss / static_cast<float>(d) + e.eps) : 1.f;
+      if (pre_gain != nullptr) {
+        // gains of this head kind and (cos, sin) of this row, precomputed
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j < P) {
-          const float a = x1[j] * inv * (kind == 0 ? gq1[j] : gk1[j]);
-          const float b = x2[j] * inv * (kind == 0 ? gq2[j] : gk2[j]);
-          float sn, cs;
-          rope_sincos(pos, rf[j], &sn, &cs);
-          x1[j] = a * cs - b * sn;
-          x2[j] = b * cs + a * sn;
+        for (int j = 0; j < 8; ++j) {
+          if (j < P) {
+            const float a = x1[j] * inv * pre_gain[c0 + j];
+            const float b = x2[j] * inv * pre_gain[half + c0 + j];
+            const float2 t = pre_cs[r * 64 + c0 + j];
+            x1[j] = a * t.x - b * t.y;
+            x2[j] = b * t.x + a * t.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j < P) {
+            const float a = x1[j] * inv * (kind == 0 ? gq1[j] : gk1[j]);
+            const float b = x2[j] * inv * (kind == 0 ? gq2[j] : gk2[j]);
+            float sn, cs;
+            rope_sincos(pos, rf[j], &sn, &cs);
+            x1[j] = a * cs - b * sn;
+            x2[j] = b * cs + a * sn;
+          }
         }
       }
     }

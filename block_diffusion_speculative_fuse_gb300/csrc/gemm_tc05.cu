@@ -53,11 +53,14 @@ struct GemmCfg {
   // Epilogue inputs loaded during the main loop (decode-sized tiles only):
   // row scales [32] and QKV routing [3][32]; the two-term BN = 16 variant
   // (O projection and down: residual epilogue) also residual rows [4][128]
-  // and the next norm's gains [128].
+  // and the next norm's gains [128]; the one-term BN = 32 variant (the QKV
+  // projection with its context rows) the q/k-norm gains [128] and the RoPE
+  // (cos, sin) of its rows [4][64].
   static constexpr bool PRE = BN <= 32;
   static constexpr bool PRE_RESID = PRE && SPLIT && BN == 16;
+  static constexpr bool PRE_ROPE = PRE && !SPLIT && BN == 32;
   static constexpr int PRE_OFF = MAIN_BYTES + 256;
-  static constexpr int PRE_BYTES = !PRE ? 0 : (PRE_RESID ? 3072 : 512);
+  static constexpr int PRE_BYTES = !PRE ? 0 : ((PRE_RESID || PRE_ROPE) ? 3072 : 512);
   static constexpr int PRE_RESID_ROWS = 4;
   static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + PRE_BYTES + 1024;  // + barriers, alignment slack
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
@@ -190,11 +193,30 @@ __global__ void __launch_bounds__(128, 1)
   int* pre_route = reinterpret_cast<int*>(smem + C::PRE_OFF + 128);      // [3][32]
   float* pre_resid = reinterpret_cast<float*>(smem + C::PRE_OFF + 512);  // [4][128]
   float* pre_g = pre_resid + C::PRE_RESID_ROWS * kTileN;                 // [128]
+  float* pre_qg = reinterpret_cast<float*>(smem + C::PRE_OFF + 512);    // [128]
+  float2* pre_cs = reinterpret_cast<float2*>(smem + C::PRE_OFF + 1024);  // [4][64]
   const int rows_mt = min(BN, p.M - blockIdx.z * BN);                    // rows of this m-tile
-  bool have_rinv = false, have_route = false, have_resid = false;
+  bool have_rinv = false, have_route = false, have_resid = false, have_rope = false;
+  int rope_rb = 0;  // first row (in the m-tile) of the RoPE table
   if constexpr (C::PRE) {
-    have_rinv = p.ssq_in != nullptr;
-    have_route = p.mode == EPI_QKV;
+    have_rinv = p.ssq_in != nullptr && (p.pre_mask & 1);
+    have_route = p.mode == EPI_QKV && (p.pre_mask & 2);
+    if constexpr (C::PRE_ROPE) {
+      // the rows this CTA will finish, as decided after the main loop
+      int rb = 0, rc = rows_mt;
+      if (p.splits > 1) {
+        if (p.cluster) {
+          const int rpc = (rows_mt + p.splits - 1) / p.splits;
+          rb = min(rows_mt, static_cast<int>(cluster_ctarank()) * rpc);
+          rc = min(rows_mt, rb + rpc) - rb;
+        } else {
+          rc = C::PRE_RESID_ROWS + 1;
+        }
+      }
+      // one head per 128-feature tile (head_dim 128): a single gain vector
+      have_rope = have_route && (p.pre_mask & 8) && rc <= C::PRE_RESID_ROWS && p.qkv.head_dim == kTileN;
+      rope_rb = rb;
+    }
     if constexpr (C::PRE_RESID) {
       // the rows this CTA will finish (as decided below): all of them, or
       // its share of a split-K cluster
@@ -209,7 +231,7 @@ __global__ void __launch_bounds__(128, 1)
           rc = C::PRE_RESID_ROWS + 1;  // the finishing CTA is known only at the end
         }
       }
-      have_resid = p.mode == EPI_RESID && rc <= C::PRE_RESID_ROWS;
+      have_resid = p.mode == EPI_RESID && (p.pre_mask & 4) && rc <= C::PRE_RESID_ROWS;
       if (have_resid && warp >= 2) {
         const int t = tid - 64;
         const int n0 = blockIdx.x * kTileN;
@@ -253,6 +275,26 @@ __global__ void __launch_bounds__(128, 1)
       if (have_route) {
         const int t = tid - 64;
         if (t < rows_mt) qkv_route(p, mt0 + t, pre_route + t, pre_route + 32 + t, pre_route + 64 + t);
+      }
+      if (have_rope) {
+        // q/k-norm gains of this tile's head(s), and (cos, sin) of every
+        // rotate-half pair at the position of each row this CTA finishes
+        // (the same rope_sincos the epilogue would call)
+        const QkvEpi& e = p.qkv;
+        const int t = tid - 64;
+        const int d = e.head_dim, half = d / 2;
+        const int head = (e.f0 + blockIdx.x * kTileN) / d;
+        const uint16_t* gsrc = head < e.n_q_heads ? e.q_norm
+                               : (head < e.n_q_heads + e.n_kv_heads ? e.k_norm : nullptr);
+        for (int f = t; f < d; f += 64) pre_qg[f] = gsrc != nullptr ? bf2f(gsrc[f]) : 1.f;
+        asm volatile("bar.sync 1, 64;" ::: "memory");  // routing of all rows written (warps 2-3)
+        int rc = min(C::PRE_RESID_ROWS, rows_mt - rope_rb);
+        for (int idx = t; idx < rc * half; idx += 64) {
+          const int r = idx / half, pr = idx % half;
+          float sn, cs;
+          rope_sincos(pre_route[32 + rope_rb + r], e.rope[pr], &sn, &cs);
+          pre_cs[r * 64 + pr] = make_float2(cs, sn);
+        }
       }
     }
   }
@@ -510,7 +552,9 @@ __global__ void __launch_bounds__(128, 1)
       case EPI_ARGMAX: epi_argmax(p, tsv, tile, m0v, rows_v, tid, sync, gridDim.x); break;
       case EPI_QKV:
         epi_qkv(p, tsv, tile, m0v, rows_v, reinterpret_cast<int*>(smem + C::SCRATCH_OFF + BN * 4), BN,
-                tid, sync, have_route ? pre_route + r_beg : nullptr, 32);
+                tid, sync, have_route ? pre_route + r_beg : nullptr, 32,
+                have_rope && r_beg == rope_rb ? pre_qg : nullptr,
+                have_rope && r_beg == rope_rb ? pre_cs : nullptr);
         break;
       default: break;
     }

@@ -109,6 +109,8 @@ struct GemmParams {
   int ld_raw;
   QkvEpi qkv;
   int dep_lead;          // < 0: signal dependents at the start; else with dep_lead k-blocks left to load
+  int pre_mask;          // epilogue inputs loaded during the main loop: 1 row scales, 2 QKV
+                         // routing, 4 residual rows, 8 QKV gains and RoPE tables
 };
 
 // Picks the MMA N width for M rows and the split-K count.
