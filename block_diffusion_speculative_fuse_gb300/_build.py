@@ -10,7 +10,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdflash_gb300.so")
 SOURCES = ["dflash_api.cu", "gemm_tc05.cu", "attention.cu", "attention_tc05.cu", "small_kernels.cu",
-           "noalloc.cu"]
+           "noalloc.cu", "sampling.cu"]
 HEADERS = ["common.cuh", "kernels.h", "epilogue.cuh", "attention.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]

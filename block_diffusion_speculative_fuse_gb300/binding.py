@@ -83,6 +83,16 @@ EXPORTS = {
     "dflash_verify_greedy": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                             ctypes.c_int32] + [ctypes.c_void_p] * 8 +
                              [ctypes.c_void_p]),
+    "dflash_sampling_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32]),
+    "dflash_verify_sampling": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p] +
+                               [ctypes.c_void_p] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
+                                                        ctypes.c_void_p]),
+    "dflash_sample_rows": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.c_void_p]),
     "dflash_target_forward": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_int32, ctypes.c_int32,
                                              ctypes.POINTER(DflashKV), ctypes.c_void_p,
@@ -210,6 +220,27 @@ def dflash_draft_block(h, anchor, anchor_pos, batch, kv: DflashKV, pending_ctx, 
         h, ptr(anchor), ptr(anchor_pos), batch, ctypes.byref(kv), ptr(pending_ctx),
         ptr(pending_req), ptr(pending_pos), T, ptr(draft), ptr(logits), ptr(hidden), ptr(ws),
         ws.numel() * ws.element_size(), stream_handle(stream)))
+
+
+def dflash_sampling_workspace_bytes(batch, B):
+    return int(load().dflash_sampling_workspace_bytes(batch, B))
+
+
+def dflash_verify_sampling(draft, draft_logits, target_logits, batch, B, vocab, temperature, u, w,
+                           out_tokens, n_accept, tgt_len_in, tgt_len_out, ctx_pending, anchor_out,
+                           anchor_pos_in, anchor_pos_out, ws, stream=None):
+    return _check("dflash_verify_sampling", load().dflash_verify_sampling(
+        ptr(draft), ptr(draft_logits), ptr(target_logits), batch, B, vocab, float(temperature),
+        ptr(u), ptr(w), ptr(out_tokens), ptr(n_accept), ptr(tgt_len_in), ptr(tgt_len_out),
+        ptr(ctx_pending), ptr(anchor_out), ptr(anchor_pos_in), ptr(anchor_pos_out), ptr(ws),
+        ws.numel() * ws.element_size(), stream_handle(stream)))
+
+
+def dflash_sample_rows(logits, n_blocks, block, skip_first, vocab, temperature, a, out, ws,
+                       stream=None):
+    return _check("dflash_sample_rows", load().dflash_sample_rows(
+        ptr(logits), n_blocks, block, skip_first, vocab, float(temperature), ptr(a), ptr(out),
+        ptr(ws), ws.numel() * ws.element_size(), stream_handle(stream)))
 
 
 def dflash_verify_greedy(draft, target, batch, B, out_tokens, n_accept, tgt_len_in,

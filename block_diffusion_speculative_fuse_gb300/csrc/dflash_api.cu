@@ -855,6 +855,54 @@ int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t ba
   return DFLASH_OK;
 }
 
+size_t dflash_sampling_workspace_bytes(int32_t batch, int32_t B) {
+  if (batch < 1 || B < 1) return 0;
+  return kHeaderBytes + al256(static_cast<size_t>(batch) * (2 * B - 1) * sizeof(double2));
+}
+
+int dflash_verify_sampling(const int32_t* draft, const float* draft_logits,
+                           const float* target_logits, int32_t batch, int32_t B, int32_t vocab,
+                           double temperature, const double* u, const double* w,
+                           int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
+                           int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
+                           const int32_t* anchor_pos_in, int32_t* anchor_pos_out, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (target_logits == nullptr || w == nullptr || out_tokens == nullptr || batch < 1 || B < 1 ||
+      B > 32 || vocab < 1 || !(temperature > 0.0) || !std::isfinite(temperature))
+    return DFLASH_ERR_INVALID_ARG;
+  if (B > 1 && (draft == nullptr || draft_logits == nullptr || u == nullptr))
+    return DFLASH_ERR_INVALID_ARG;
+  if ((tgt_len_out != nullptr && tgt_len_in == nullptr) ||
+      (anchor_pos_out != nullptr && anchor_pos_in == nullptr))
+    return DFLASH_ERR_INVALID_ARG;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255)) return DFLASH_ERR_INVALID_ARG;
+  if (ws_bytes < dflash_sampling_workspace_bytes(batch, B)) return DFLASH_ERR_CAPACITY;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  DF_CUDA(verify_sampling_launch(draft, draft_logits, target_logits, batch, B, vocab, temperature,
+                                 u, w, reinterpret_cast<double2*>(base + kHeaderBytes), out_tokens,
+                                 n_accept, tgt_len_in, tgt_len_out, ctx_pending, anchor_out,
+                                 anchor_pos_in, anchor_pos_out, reinterpret_cast<int32_t*>(base),
+                                 static_cast<cudaStream_t>(stream), true));
+  return DFLASH_OK;
+}
+
+int dflash_sample_rows(const float* logits, int32_t n_blocks, int32_t block, int32_t skip_first,
+                       int32_t vocab, double temperature, const double* a, int32_t* out,
+                       void* ws, size_t ws_bytes, void* stream) {
+  if (logits == nullptr || a == nullptr || out == nullptr || n_blocks < 1 || block < 1 ||
+      (skip_first != 0 && skip_first != 1) || block - skip_first < 1 || vocab < 1 ||
+      !(temperature > 0.0) || !std::isfinite(temperature))
+    return DFLASH_ERR_INVALID_ARG;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255)) return DFLASH_ERR_INVALID_ARG;
+  const size_t used = static_cast<size_t>(n_blocks) * (block - skip_first);
+  if (used > (1u << 30) || ws_bytes < kHeaderBytes + al256(used * sizeof(double2)))
+    return DFLASH_ERR_CAPACITY;
+  DF_CUDA(sample_rows_launch(logits, static_cast<int>(used), block, skip_first, vocab, temperature,
+                             a, reinterpret_cast<double2*>(static_cast<uint8_t*>(ws) + kHeaderBytes),
+                             out, static_cast<cudaStream_t>(stream), true));
+  return DFLASH_OK;
+}
+
 int dflash_target_forward(dflash_model m, const int32_t* tokens, const int32_t* pos0,
                           int32_t batch, int32_t n, const dflash_kv* kv,
                           const int32_t* tap_layers, int32_t n_taps, void* taps,

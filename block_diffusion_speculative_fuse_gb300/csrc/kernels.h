@@ -204,6 +204,20 @@ cudaError_t synth_target_launch(const int32_t* draft, int batch, int B, const ui
                                 int vocab, uint64_t seed, int64_t* step, int advance,
                                 int32_t* target, cudaStream_t s, bool pdl);
 cudaError_t copy_rows_f32_launch(const float* src, float* dst, size_t n, cudaStream_t s, bool pdl);
+// sampling.cu: verify at temperature T > 0 (stats: batch*(2B-1) double2), and
+// categorical draws from softmax(logits / T) of the used rows of a blocked
+// logits array (stats: n_used double2)
+cudaError_t verify_sampling_launch(const int32_t* draft, const float* q_rows, const float* p_rows,
+                                   int batch, int B, int V, double T, const double* u,
+                                   const double* w, double2* stats, int32_t* out_tokens,
+                                   int32_t* n_accept, const int32_t* tgt_len_in,
+                                   int32_t* tgt_len_out, int32_t* ctx_pending,
+                                   int32_t* anchor_out, const int32_t* anchor_pos_in,
+                                   int32_t* anchor_pos_out, int32_t* status, cudaStream_t s,
+                                   bool pdl);
+cudaError_t sample_rows_launch(const float* rows, int n_used, int block, int skip, int V, double T,
+                               const double* a, double2* stats, int32_t* out, cudaStream_t s,
+                               bool pdl);
 cudaError_t wait_selftest_launch(int arrive, uint64_t limit_ns, int* status, int64_t* waited_ns,
                                  cudaStream_t s);
 

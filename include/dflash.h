@@ -242,6 +242,51 @@ int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t ba
                          int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
                          const int32_t* anchor_pos_in, int32_t* anchor_pos_out, void* stream);
 
+/* Verification at temperature T > 0 ("DFlash: how block diffusion boosts
+ * NVIDIA Blackwell throughput", section "Real-world integration": sampling-
+ * mode speedups; introduction: lossless).  The pages state no rule; this is
+ * the standard lossless speculative-sampling rule applied per block
+ * position, the drafts d_i having been drawn independently from
+ * q_i = softmax(z_i / T) (dflash_sample_rows):
+ *   accept d_i while u_i * q_i(d_i) < p_i(d_i), p_j = softmax(y_j / T);
+ *   at the first rejection emit a draw from max(0, p_i - q_i), after B-1
+ *   acceptances a draw from p_B.
+ * draft int32 [batch][B-1]; draft_logits fp32 [batch][B][vocab] as
+ * dflash_draft_block writes them (block row 0, the anchor, is not read; row
+ * i+1 gives q for draft i); target_logits fp32 [batch][B][vocab] (row j-1 =
+ * the target's logits for block position j); u fp64 [batch][B-1] acceptance
+ * uniforms, w fp64 [batch][B] uniforms of the emitted draw at each position
+ * (w[r][B-1]: the bonus); all in [0, 1).  A draw with uniform a returns the
+ * smallest k with a*S < C_k (C the running sum of the weights, S the total).
+ * Outputs as in dflash_verify_greedy; out_tokens is required, the others
+ * may be NULL.  Arithmetic: fp32 exponentials of (z - max)/T, fp64 sums and
+ * running sums in a fixed order, fp64 exp for the accept test; a decision
+ * can differ from exact arithmetic only when its uniform lies within about
+ * 1e-6 (relative) of the boundary.  Deterministic.  ws: 256-byte aligned,
+ * at least dflash_sampling_workspace_bytes(batch, B), initialised with
+ * dflash_workspace_init; a draft token outside [0, vocab) is rejected and
+ * recorded as DFLASH_ERR_INVALID_ARG (site 401) in its status word.
+ * batch >= 1, 1 <= B <= 32, temperature finite and > 0. */
+size_t dflash_sampling_workspace_bytes(int32_t batch, int32_t B);
+int dflash_verify_sampling(const int32_t* draft, const float* draft_logits,
+                           const float* target_logits, int32_t batch, int32_t B, int32_t vocab,
+                           double temperature, const double* u, const double* w,
+                           int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
+                           int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
+                           const int32_t* anchor_pos_in, int32_t* anchor_pos_out, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* Draft sampling for the temperature-T verify: one categorical draw from
+ * softmax(z / T) per used row of logits fp32 [n_blocks][block][vocab] (with
+ * skip_first = 1 the first row of every block is not used, as for the
+ * drafter's anchor row); out int32 and a fp64 uniforms in [0, 1), both
+ * indexed by used row ([n_blocks][block - skip_first]).  Same draw and
+ * arithmetic as dflash_verify_sampling; ws as there, sized for
+ * n_blocks*(block - skip_first) rows (64 KiB + 16 bytes per row). */
+int dflash_sample_rows(const float* logits, int32_t n_blocks, int32_t block, int32_t skip_first,
+                       int32_t vocab, double temperature, const double* a, int32_t* out,
+                       void* ws, size_t ws_bytes, void* stream);
+
 /* ----------------------------------------------- end-to-end loop helpers */
 
 /* Causal target forward over `batch` requests x `n` consecutive rows

@@ -113,3 +113,25 @@ def test_selftest_wait_rejects_bad_args_before_launch(lib):
     assert lib.dflash_selftest_wait(0, 0, None, ws, 1 << 16, None) == -1
     assert lib.dflash_selftest_wait(0, 10**9 + 1, None, ws, 1 << 16, None) == -1
     assert lib.dflash_selftest_wait(0, 1000, ctypes.c_void_p(4), ws, 1 << 16, None) == -1
+
+
+def test_sampling_calls_reject_bad_args_before_launch(lib):
+    d = ctypes.c_void_p(0x1000)
+    ws = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails its checks
+    need = lib.dflash_sampling_workspace_bytes(2, 16)
+    assert need == 64 * 1024 + ((2 * 31 * 16 + 255) // 256) * 256
+    assert lib.dflash_sampling_workspace_bytes(0, 16) == 0
+    f = lib.dflash_verify_sampling
+    ok = [d, d, d, 2, 16, 1000, 0.7, d, d] + [d] + [None] * 7
+    assert f(*ok[:6], 0.0, *ok[7:], ws, need, None) == -1          # T = 0
+    assert f(*ok[:6], float("nan"), *ok[7:], ws, need, None) == -1
+    assert f(*ok[:3], 2, 33, *ok[5:], ws, need, None) == -1        # B > 32
+    assert f(None, *ok[1:], ws, need, None) == -1                  # drafts missing (B > 1)
+    assert f(*ok[:9], None, *ok[10:], ws, need, None) == -1        # out_tokens missing
+    assert f(*ok, ctypes.c_void_p((1 << 20) + 8), need, None) == -1  # misaligned workspace
+    assert f(*ok, ws, need - 1, None) == -3                        # workspace too small
+    g = lib.dflash_sample_rows
+    assert g(d, 2, 16, 2, 1000, 0.7, d, d, ws, need, None) == -1   # skip_first not 0/1
+    assert g(d, 2, 1, 1, 1000, 0.7, d, d, ws, need, None) == -1    # no used rows
+    assert g(d, 2, 16, 1, 1000, -1.0, d, d, ws, need, None) == -1  # T < 0
+    assert g(d, 2, 16, 1, 1000, 0.7, d, d, ws, 1024, None) == -3   # workspace too small
