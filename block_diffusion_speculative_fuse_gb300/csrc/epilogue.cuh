@@ -79,15 +79,30 @@ __device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int 
   if (pre_resid != nullptr) {
     for (int r = 0; r < rows; ++r) ts[r * kTsLd + f] += pre_resid[r * kTileN + f];
   } else {
-    for (int r0 = 0; r0 < rows; r0 += 16) {
-      float v[16];
+    // the tile's residual rows as 16-byte pieces, 16 loads in flight per
+    // thread, added where they land (then every column is complete)
+    const float* rbase = p.resid + static_cast<size_t>(m0) * p.ld_resid + tile * kTileN;
+    const int pieces = rows * (kTileN / 4);
+    for (int c0 = tid; c0 < pieces; c0 += 128 * 16) {
+      float4 v[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        v[j] = (r0 + j < rows) ? __ldcg(p.resid + static_cast<size_t>(m0 + r0 + j) * p.ld_resid + n) : 0.f;
+      for (int i = 0; i < 16; ++i) {
+        const int c = c0 + i * 128;
+        if (c < pieces)
+          v[i] = __ldcg(reinterpret_cast<const float4*>(rbase + static_cast<size_t>(c / 32) * p.ld_resid) + c % 32);
+      }
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (r0 + j < rows) ts[(r0 + j) * kTsLd + f] += v[j];
+      for (int i = 0; i < 16; ++i) {
+        const int c = c0 + i * 128;
+        if (c < pieces) {
+          float4* t = reinterpret_cast<float4*>(ts + (c / 32) * kTsLd + (c % 32) * 4);
+          float4 x = *t;
+          x.x += v[i].x; x.y += v[i].y; x.z += v[i].z; x.w += v[i].w;
+          *t = x;
+        }
+      }
     }
+    sync();
   }
   if (p.conv != nullptr && p.conv_width > 0) {
     const int c = (p.conv_width - 1) / 2;

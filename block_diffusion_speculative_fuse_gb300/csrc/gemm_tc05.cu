@@ -86,7 +86,11 @@ __global__ void __launch_bounds__(128, 1)
   float* ts = reinterpret_cast<float*>(smem);  // staged tile (after the mainloop)
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int tile = blockIdx.x, split = blockIdx.y, mt = blockIdx.z;
+  // grid (m-tiles, splits, n-tiles): the m-tiles of one weight tile are
+  // consecutive CTAs (clusters), so they stream the same weight rows together
+  // and the second one reads them from L2
+  const int tile = blockIdx.z, split = blockIdx.y, mt = blockIdx.x;
+  const int n_tiles = gridDim.z;
   const int m0 = mt * BN;
   const int kb0 = split * p.kb_per_split;
   const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
@@ -195,7 +199,7 @@ __global__ void __launch_bounds__(128, 1)
   float* pre_g = pre_resid + C::PRE_RESID_ROWS * kTileN;                 // [128]
   float* pre_qg = reinterpret_cast<float*>(smem + C::PRE_OFF + 512);    // [128]
   float2* pre_cs = reinterpret_cast<float2*>(smem + C::PRE_OFF + 1024);  // [4][64]
-  const int rows_mt = min(BN, p.M - blockIdx.z * BN);                    // rows of this m-tile
+  const int rows_mt = min(BN, p.M - mt * BN);                            // rows of this m-tile
   bool have_rinv = false, have_route = false, have_resid = false, have_rope = false;
   int rope_rb = 0;  // first row (in the m-tile) of the RoPE table
   if constexpr (C::PRE) {
@@ -234,11 +238,11 @@ __global__ void __launch_bounds__(128, 1)
       have_resid = p.mode == EPI_RESID && (p.pre_mask & 4) && rc <= C::PRE_RESID_ROWS;
       if (have_resid && warp >= 2) {
         const int t = tid - 64;
-        const int n0 = blockIdx.x * kTileN;
+        const int n0 = tile * kTileN;
         for (int idx = t; idx < rc * (kTileN / 4); idx += 64) {
           const int r = idx / (kTileN / 4), c4 = idx % (kTileN / 4);
           *reinterpret_cast<float4*>(pre_resid + r * kTileN + c4 * 4) = __ldcg(
-              reinterpret_cast<const float4*>(p.resid + static_cast<size_t>(blockIdx.z * BN + rb + r) * p.ld_resid + n0) + c4);
+              reinterpret_cast<const float4*>(p.resid + static_cast<size_t>(mt * BN + rb + r) * p.ld_resid + n0) + c4);
         }
         if (p.gnext != nullptr)
           for (int f = t; f < kTileN; f += 64) pre_g[f] = bf2f(p.gnext[n0 + f]);
@@ -246,7 +250,7 @@ __global__ void __launch_bounds__(128, 1)
     }
     if (warp >= 2) {
       const int w2 = warp - 2;
-      const int mt0 = blockIdx.z * BN;
+      const int mt0 = mt * BN;
       if (have_rinv) {
         // row r's sum: lane t adds tiles t, t+32, ... in order, then the xor
         // butterfly of warp_sum (as in the epilogue below); rows w2, w2+2, ...
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(128, 1)
         const QkvEpi& e = p.qkv;
         const int t = tid - 64;
         const int d = e.head_dim, half = d / 2;
-        const int head = (e.f0 + blockIdx.x * kTileN) / d;
+        const int head = (e.f0 + tile * kTileN) / d;
         const uint16_t* gsrc = head < e.n_q_heads ? e.q_norm
                                : (head < e.n_q_heads + e.n_kv_heads ? e.k_norm : nullptr);
         for (int f = t; f < d; f += 64) pre_qg[f] = gsrc != nullptr ? bf2f(gsrc[f]) : 1.f;
@@ -348,7 +352,7 @@ __global__ void __launch_bounds__(128, 1)
     }
     __syncthreads();
     if (tid == 0) {
-      const int prev = aborted ? 0 : atomicAdd(&p.counters[mt * gridDim.x + tile], 1);
+      const int prev = aborted ? 0 : atomicAdd(&p.counters[mt * n_tiles + tile], 1);
       *last_flag = (!aborted && prev == p.splits - 1) ? 1 : 0;
     }
     __syncthreads();
@@ -400,7 +404,7 @@ __global__ void __launch_bounds__(128, 1)
             *reinterpret_cast<float4*>(ts + (c / 32) * C::TS_LD + (c % 32) * 4) = acc[i];
         }
       }
-      if (tid == 0) p.counters[mt * gridDim.x + tile] = 0;
+      if (tid == 0) p.counters[mt * n_tiles + tile] = 0;
       __syncthreads();
       do_epi = true;
     }
@@ -549,7 +553,7 @@ __global__ void __launch_bounds__(128, 1)
                   have_resid && p.gnext != nullptr ? pre_g : nullptr);
         break;
       case EPI_SWIGLU: epi_swiglu(p, tsv, tile, m0v, rows_v, tid, sync); break;
-      case EPI_ARGMAX: epi_argmax(p, tsv, tile, m0v, rows_v, tid, sync, gridDim.x); break;
+      case EPI_ARGMAX: epi_argmax(p, tsv, tile, m0v, rows_v, tid, sync, n_tiles); break;
       case EPI_QKV:
         epi_qkv(p, tsv, tile, m0v, rows_v, reinterpret_cast<int*>(smem + C::SCRATCH_OFF + BN * 4), BN,
                 tid, sync, have_route ? pre_route + r_beg : nullptr, 32,
@@ -638,7 +642,7 @@ static cudaError_t launch_bn(const CUtensorMap* w_map, const CUtensorMap* x_map,
     attr_device = dev;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.N / kTileN, p.splits, (p.M + BN - 1) / BN);
+  cfg.gridDim = dim3((p.M + BN - 1) / BN, p.splits, p.N / kTileN);
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;

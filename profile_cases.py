@@ -1,11 +1,17 @@
-"""Small, self-contained launch cases for profiling single kernels with ncu.
+"""Small, self-contained launch cases for profiling kernels with ncu.
 
-    python profile_cases.py lm_head
+    python profile_cases.py lm_head [--rows 16]
     python profile_cases.py step [--config NAME]
+    python profile_cases.py target [--iters 2]
+    python profile_cases.py sampling
 
 lm_head: the shared LM head + argmax of the Qwen3-8B-shaped drafter
-(151936 x 4096 bf16 weights, 16 rows), launched a few times, ~1.7 GB on the
-device.  step: a few eager draft steps of a workload (default qwen3_8b_b1).
+(151936 x 4096 bf16 weights, `rows` rows), launched a few times, ~1.7 GB on
+the device.  step: a few eager draft steps of a workload (default
+qwen3_8b_b1).  target: block-verify passes of the end-to-end workload's
+8-layer H=4096 target (batch 8 x 16 rows, context 1024), ~5 GB.  sampling:
+draft sampling and the temperature-1 verify at batch 32, block 16, vocab
+151936 (random logits, ~0.7 GB).
 """
 import argparse
 import os
@@ -50,16 +56,55 @@ def step(config="qwen3_8b_b1", iters=3):
     print("step ok", st.n_accept.tolist()[:4])
 
 
+def target(iters=2, batch=8, ctx=1024, n=16):
+    from block_diffusion_speculative_fuse_gb300.device import i32
+    from block_diffusion_speculative_fuse_gb300.generate import TargetRunner
+    wl = W.get_workload("e2e_8layer")
+    ts = wl.target
+    m = DeviceModel(ts, W.target_weights(ts, wl.wid), W.shared_weights(ts, wl.wid), draft=False)
+    run = TargetRunner(m, batch, ctx + n + 1, n, wl.tap_layers)
+    toks = i32(W.uniform_tokens(batch * n, ts.vocab, wl.wid, 99).reshape(batch, n))
+    pos = i32(np.full(batch, ctx))
+    for _ in range(iters):
+        out, _ = run.forward(toks, pos, n, want_taps=True)
+    torch.cuda.synchronize()
+    print("target ok", out[0, :4].tolist())
+
+
+def sampling(iters=2, batch=32, block=16, vocab=151936):
+    g = np.random.default_rng(3)
+    z = torch.from_numpy((g.standard_normal((batch, block, vocab)) * 1.3).astype(np.float32)).cuda()
+    y = torch.from_numpy((g.standard_normal((batch, block, vocab)) * 1.3).astype(np.float32)).cuda()
+    a = torch.from_numpy(g.random((batch, block))).cuda()
+    d = torch.zeros((batch, block - 1), dtype=torch.int32, device="cuda")
+    out = torch.zeros((batch, block), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(B.dflash_sampling_workspace_bytes(batch, block), dtype=torch.uint8,
+                     device="cuda")
+    B.dflash_workspace_init(ws)
+    for _ in range(iters):
+        B.dflash_sample_rows(z, batch, block, 1, vocab, 1.0, a, d, ws)
+        B.dflash_verify_sampling(d, z, y, batch, block, vocab, 1.0, a, a, out, None, None, None,
+                                 None, None, None, None, ws)
+    torch.cuda.synchronize()
+    assert B.dflash_get_status(ws)[0] == 0
+    print("sampling ok", out[0, :4].tolist())
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["lm_head", "step"])
+    ap.add_argument("case", choices=["lm_head", "step", "target", "sampling"])
     ap.add_argument("--config", default="qwen3_8b_b1")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--rows", type=int, default=16)
     a = ap.parse_args()
     _build.build()
     B.load()
     if a.case == "lm_head":
-        lm_head(a.iters)
+        lm_head(a.iters, a.rows)
+    elif a.case == "target":
+        target(a.iters)
+    elif a.case == "sampling":
+        sampling(a.iters)
     else:
         step(a.config, a.iters)
 
