@@ -81,13 +81,13 @@ EXPORTS = {
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                           ctypes.c_void_p]),
     "dflash_verify_greedy": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
-                                            ctypes.c_int32] + [ctypes.c_void_p] * 8 +
+                                            ctypes.c_int32] + [ctypes.c_void_p] * 9 +
                              [ctypes.c_void_p]),
     "dflash_sampling_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32]),
     "dflash_verify_sampling": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                               ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p] +
-                               [ctypes.c_void_p] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
+                               [ctypes.c_void_p] * 9 + [ctypes.c_void_p, ctypes.c_size_t,
                                                         ctypes.c_void_p]),
     "dflash_sample_rows": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
@@ -228,12 +228,12 @@ def dflash_sampling_workspace_bytes(batch, B):
 
 def dflash_verify_sampling(draft, draft_logits, target_logits, batch, B, vocab, temperature, u, w,
                            out_tokens, n_accept, tgt_len_in, tgt_len_out, ctx_pending, anchor_out,
-                           anchor_pos_in, anchor_pos_out, ws, stream=None):
+                           anchor_pos_in, anchor_pos_out, ws, stream=None, ctx_pos=None):
     return _check("dflash_verify_sampling", load().dflash_verify_sampling(
         ptr(draft), ptr(draft_logits), ptr(target_logits), batch, B, vocab, float(temperature),
         ptr(u), ptr(w), ptr(out_tokens), ptr(n_accept), ptr(tgt_len_in), ptr(tgt_len_out),
-        ptr(ctx_pending), ptr(anchor_out), ptr(anchor_pos_in), ptr(anchor_pos_out), ptr(ws),
-        ws.numel() * ws.element_size(), stream_handle(stream)))
+        ptr(ctx_pending), ptr(anchor_out), ptr(anchor_pos_in), ptr(anchor_pos_out), ptr(ctx_pos),
+        ptr(ws), ws.numel() * ws.element_size(), stream_handle(stream)))
 
 
 def dflash_sample_rows(logits, n_blocks, block, skip_first, vocab, temperature, a, out, ws,
@@ -245,11 +245,11 @@ def dflash_sample_rows(logits, n_blocks, block, skip_first, vocab, temperature, 
 
 def dflash_verify_greedy(draft, target, batch, B, out_tokens, n_accept, tgt_len_in,
                          tgt_len_out, ctx_pending, anchor_out, anchor_pos_in, anchor_pos_out,
-                         stream=None):
+                         stream=None, ctx_pos=None):
     return _check("dflash_verify_greedy", load().dflash_verify_greedy(
         ptr(draft), ptr(target), batch, B, ptr(out_tokens), ptr(n_accept), ptr(tgt_len_in),
         ptr(tgt_len_out), ptr(ctx_pending), ptr(anchor_out), ptr(anchor_pos_in),
-        ptr(anchor_pos_out), stream_handle(stream)))
+        ptr(anchor_pos_out), ptr(ctx_pos), stream_handle(stream)))
 
 
 def dflash_target_forward(h, tokens, pos0, batch, n, kv: DflashKV, tap_layers, n_taps, taps,

@@ -40,31 +40,37 @@ namespace {
 
 constexpr int kChunkKeys = 64;
 constexpr int kChunkPages = 4;
-constexpr int kStages = 4;
 constexpr int kMaxPagesTc = 1024;  // pages per split (staged ids)
+// causal (target) key splits: fixed 512-key boundaries, so a row's result
+// does not depend on the batch or the number of rows of the call
+constexpr int kTargetSplitPagesTc = 32;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kThreads = 192;      // warps 0-3 softmax, 4 TMA, 5 MMA
 
-template <int D>
+// TERMS = 2: every key chunk also carries the low bf16 terms of K and V
+// (planes K, V, K_lo, V_lo in a stage, as in the pool's pages).
+template <int D, int TERMS = 1>
 struct TcCfg {
+  static constexpr int STAGES = TERMS == 2 ? 2 : 4;
+  static constexpr int PLANES = 2 * TERMS;
   static constexpr int HALVES = D / 64;
   static constexpr int Q_BYTES = 128 * D * 2;                   // [HALVES][128 rows][64]
   static constexpr int P_BYTES = 128 * kChunkKeys * 2;          // [128 rows][64 keys]
   static constexpr int KV_HALF = kChunkKeys * 64 * 2;           // [64 keys][64 cols] = 8 KB
   static constexpr int K_BYTES = kChunkKeys * D * 2;            // [HALVES][64][64]
-  static constexpr int STAGE_BYTES = 2 * K_BYTES;               // K then V
-  static constexpr int BOXES = kChunkPages * 2 * HALVES;        // TMA boxes per chunk
+  static constexpr int STAGE_BYTES = PLANES * K_BYTES;          // K, V (, K_lo, V_lo)
+  static constexpr int BOXES = kChunkPages * PLANES * HALVES;   // TMA boxes per chunk
   static constexpr int Q_OFF = 0;
   static constexpr int P_OFF = Q_OFF + Q_BYTES;
   static constexpr int KV_OFF = P_OFF + 2 * P_BYTES;
-  static constexpr int PG_OFF = KV_OFF + kStages * STAGE_BYTES;
+  static constexpr int PG_OFF = KV_OFF + STAGES * STAGE_BYTES;
   static constexpr int PN_OFF = PG_OFF + kMaxPagesTc * 4;
   static constexpr int BAR_OFF = PN_OFF + kMaxPagesTc * 4;
   static constexpr int SMEM = BAR_OFF + 512 + 1024;             // barriers + alignment slack
   // combine staging (after the key loop, in the K/V stage area): 128 row slots
   // merge staging: at most 160 partial rows (rows per CTA x parts x splits
   // <= (R + splits) x parts) of D + 4 floats plus (m, l)
-  static_assert(160 * ((D + 4) * 4 + 8) <= kStages * STAGE_BYTES, "merge staging must fit");
+  static_assert(160 * ((D + 4) * 4 + 8) <= STAGES * STAGE_BYTES, "merge staging must fit");
   static_assert(BOXES <= 32, "one TMA box per producer lane");
   static constexpr uint32_t TMEM_COLS = 256;                    // S0 | S1 | O
   static constexpr uint32_t S_COL0 = 0, O_COL = 128;
@@ -83,13 +89,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int D>
+// CAUSAL (the target's verify / decode pass): block row i of the CTA's query
+// tile sits at position pos0 + i and attends to pool keys [0, pos0 + i] (its
+// own K/V were written to the pool by the QKV epilogue); there are no
+// separate block keys.  The CTA takes block rows [qt*rpt, (qt+1)*rpt) of its
+// request (p.rows_per_tile), so a row's arithmetic never depends on how many
+// rows the call has.
+template <int D, bool CAUSAL = false, int TERMS = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_kernel(const __grid_constant__ CUtensorMap pool_map,
                      const __grid_constant__ CUtensorMap kblk_map,
                      const __grid_constant__ CUtensorMap vblk_map,
                      const __grid_constant__ AttnTcParams p) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, TERMS>;
+  constexpr int kStages = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -108,7 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int split = blockIdx.x;
   const int req = blockIdx.y / p.hkv, g = blockIdx.y % p.hkv;
   const int G = p.hq / p.hkv;
-  const int R = p.n * G;                        // real query rows (<= 128)
+  const int i0 = blockIdx.z * p.rows_per_tile;  // first block row of this query tile
+  const int n_here = max(0, min(p.n, i0 + p.rows_per_tile) - i0);
+  const int R = n_here * G;                     // real query rows (<= 128)
   const bool dual = R <= 64;                    // two warp pairs, two softmax states
   const int n_act = (R + 31) / 32;              // warps (per pair when dual) with real rows
 
@@ -161,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = idx / QCH, c = idx % QCH;
     qv[k] = make_uint4(0u, 0u, 0u, 0u);
     if (idx < qrows * QCH && row < R) {
-      const int i = row / G, h = row % G;
+      const int i = i0 + row / G, h = row % G;
       qv[k] = __ldcg(reinterpret_cast<const uint4*>(
           p.q + ((static_cast<size_t>(req) * p.n + i) * p.hq + g * G + h) * D + c * 8));
     }
@@ -177,8 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   // ---- key space of this request: context pages [0, Pc), then block pages
-  const int Pc = (L + 15) / 16;
-  const int Pb = (p.n + 15) / 16;
+  // (causal: pool pages up to the tile's last row, no block pages)
+  const int Lk = CAUSAL ? L + i0 + n_here : L;
+  const int Pc = (Lk + 15) / 16;
+  const int Pb = CAUSAL ? 0 : (p.n + 15) / 16;
   const int pg_hi = min(Pc + Pb, pg_lo + p.split_pages);
   const int npg = max(0, pg_hi - pg_lo);
   const int nch = (npg + kChunkPages - 1) / kChunkPages;
@@ -194,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           raise_status(p.status, DFLASH_ERR_CAPACITY, 301);
           id = -1;
         } else {
-          cnt = min(16, L - j * 16);
+          cnt = min(16, Lk - j * 16);
         }
       } else {
         id = -2 - (j - Pc);
@@ -229,12 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if (lane < C::BOXES) {
-        const int pp = lane / (2 * C::HALVES), kv = (lane / C::HALVES) % 2, hf = lane % C::HALVES;
+        // lane -> (page, plane, 64-column half); planes K, V (, K_lo, V_lo)
+        const int pp = lane / (C::PLANES * C::HALVES), kv = (lane / C::HALVES) % C::PLANES,
+                  hf = lane % C::HALVES;
         const int id = pages_s[c * kChunkPages + pp];
         const CUtensorMap* map = &pool_map;
         int y;
         if (id >= 0) {
-          y = p.pool_row0 + (id * 2 * p.hkv + g) * 16 + kv * p.hkv * 16;
+          y = p.pool_row0 + ((id * C::PLANES + kv) * p.hkv + g) * 16;
         } else if (id <= -2) {
           map = kv ? &vblk_map : &kblk_map;
           y = (req * p.hkv + g) * p.n + (-2 - id) * 16;
@@ -266,11 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sm + C::KV_OFF + st * C::STAGE_BYTES);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k % 4) * 32;  // 16 K-elements within the 128-B row
-          const uint64_t ad = umma_desc_sw128(q_addr + (k / 4) * (128 * 128) + off);
-          const uint64_t bd = umma_desc_sw128(k_addr + (k / 4) * C::KV_HALF + off);
-          umma_bf16(tmem + C::S_COL0 + b * kChunkKeys, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+        for (int t = 0; t < TERMS; ++t) {
+          // S = Q K^T (+ Q K_lo^T: plane 2 of the stage)
+          const uint32_t kt = k_addr + t * 2 * C::K_BYTES;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k % 4) * 32;  // 16 K-elements within the 128-B row
+            const uint64_t ad = umma_desc_sw128(q_addr + (k / 4) * (128 * 128) + off);
+            const uint64_t bd = umma_desc_sw128(kt + (k / 4) * C::KV_HALF + off);
+            umma_bf16(tmem + C::S_COL0 + b * kChunkKeys, ad, bd, idesc_s, (t | k) > 0 ? 1u : 0u);
+          }
         }
         umma_commit(&s_full[b]);
         return true;
@@ -282,11 +306,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t p_addr = smem_u32(sm + C::P_OFF + b * C::P_BYTES);
         const uint32_t v_addr = smem_u32(sm + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES);
 #pragma unroll
-        for (int k = 0; k < kChunkKeys / 16; ++k) {
-          const uint64_t ad = umma_desc_sw128(p_addr + k * 32);
-          // keys 16k..16k+15 = rows of the V tile; d halves are C::KV_HALF apart
-          const uint64_t bd = umma_desc_sw128_mn(v_addr + k * 16 * 128, C::KV_HALF, 1024);
-          umma_bf16(tmem + C::O_COL, ad, bd, idesc_pv, (c > 0 || k > 0) ? 1u : 0u);
+        for (int t = 0; t < TERMS; ++t) {
+          // O += P V (+ P V_lo: plane 3 of the stage)
+          const uint32_t vt = v_addr + t * 2 * C::K_BYTES;
+#pragma unroll
+          for (int k = 0; k < kChunkKeys / 16; ++k) {
+            const uint64_t ad = umma_desc_sw128(p_addr + k * 32);
+            // keys 16k..16k+15 = rows of the V tile; d halves are C::KV_HALF apart
+            const uint64_t bd = umma_desc_sw128_mn(vt + k * 16 * 128, C::KV_HALF, 1024);
+            umma_bf16(tmem + C::O_COL, ad, bd, idesc_pv, (c > 0 || t > 0 || k > 0) ? 1u : 0u);
+          }
         }
         umma_commit(&pv_done[b]);
         umma_commit(&kv_empty[st]);
@@ -348,6 +377,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 64; ++j) s[j] = ((j % 16) < cntp[j / 16]) ? s[j] : -INFINITY;
       }
+      if constexpr (CAUSAL) {
+        // keys past this row's own position
+        const int kpos0 = (pg_lo + c * kChunkPages) * 16;
+        const int qpos = L + i0 + row_l / G;
+        if (kpos0 + 63 > qpos) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) s[j] = (kpos0 + j <= qpos) ? s[j] : -INFINITY;
+        }
+      }
       float mx8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(s[e], s[e + 8]);
@@ -408,13 +446,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
       if (stale) {
         // rows past a context page's valid keys hold stale pool data: zero
-        // their V rows so that 0 * V stays 0
+        // their V rows (and low terms) so that 0 * V stays 0
         uint8_t* vst = sm + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
         for (int idx = row_l; idx < kChunkKeys * C::HALVES * 8; idx += n_act * 32) {
           const int key = idx / (C::HALVES * 8), rem = idx % (C::HALVES * 8);
           const int hf = rem / 8, c16 = rem % 8;
-          if ((key % 16) >= cntp[key / 16])
+          if ((key % 16) >= cntp[key / 16]) {
             *reinterpret_cast<uint4*>(vst + hf * C::KV_HALF + swz128(key, c16)) = make_uint4(0u, 0u, 0u, 0u);
+            if (TERMS == 2)
+              *reinterpret_cast<uint4*>(vst + 2 * C::K_BYTES + hf * C::KV_HALF + swz128(key, c16)) =
+                  make_uint4(0u, 0u, 0u, 0u);
+          }
         }
       }
       fence_proxy_async_smem();
@@ -562,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float inv = 1.f / lsum;
-      const int i = r / G, h = r % G;
+      const int i = i0 + r / G, h = r % G;
       const size_t ob = ((static_cast<size_t>(req) * p.n + i) * p.hq + g * G + h) * D + lane * VEC;
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
@@ -578,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D>
+template <int D, bool CAUSAL, int TERMS>
 cudaError_t launch_tc(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
                       const CUtensorMap* vblk_map, const AttnTcParams& p, cudaStream_t s,
                       bool pdl) {
@@ -586,10 +628,12 @@ cudaError_t launch_tc(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc05_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc05_kernel<D, CAUSAL, TERMS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TcCfg<D, TERMS>::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_tc05_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(attn_tc05_kernel<D, CAUSAL, TERMS>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_device = dev;
   }
@@ -606,14 +650,15 @@ cudaError_t launch_tc(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
   attrs[na].val.clusterDim.z = 1;
   ++na;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_splits, p.batch * p.hkv, 1);
+  cfg.gridDim = dim3(p.n_splits, p.batch * p.hkv, (p.n + p.rows_per_tile - 1) / p.rows_per_tile);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = TcCfg<D>::SMEM;
+  cfg.dynamicSmemBytes = TcCfg<D, TERMS>::SMEM;
   cfg.stream = s;
   cfg.attrs = attrs;
   cfg.numAttrs = na;
   count_launch();
-  return cudaLaunchKernelEx(&cfg, attn_tc05_kernel<D>, *pool_map, *kblk_map, *vblk_map, p);
+  return cudaLaunchKernelEx(&cfg, attn_tc05_kernel<D, CAUSAL, TERMS>, *pool_map, *kblk_map,
+                            *vblk_map, p);
 }
 
 }  // namespace
@@ -690,9 +735,25 @@ cudaError_t attention_tc_launch(const CUtensorMap* pool_map, const CUtensorMap* 
                                 const CUtensorMap* vblk_map, const AttnTcParams& p,
                                 cudaStream_t s, bool pdl) {
   if (p.n_splits < 1 || p.n_splits > kMaxAttnCluster) return cudaErrorInvalidValue;
-  if (p.d == 128) return launch_tc<128>(pool_map, kblk_map, vblk_map, p, s, pdl);
-  if (p.d == 64) return launch_tc<64>(pool_map, kblk_map, vblk_map, p, s, pdl);
+  if (p.rows_per_tile < 1 || p.rows_per_tile * (p.hq / p.hkv) > 128) return cudaErrorInvalidValue;
+  if (p.causal) {
+    // the target path: dual-state query tiles only, one- or two-term K/V
+    if (p.rows_per_tile * (p.hq / p.hkv) > 64) return cudaErrorInvalidValue;
+    if (p.kv_terms == 2) {
+      if (p.d == 128) return launch_tc<128, true, 2>(pool_map, kblk_map, vblk_map, p, s, pdl);
+      if (p.d == 64) return launch_tc<64, true, 2>(pool_map, kblk_map, vblk_map, p, s, pdl);
+    } else {
+      if (p.d == 128) return launch_tc<128, true, 1>(pool_map, kblk_map, vblk_map, p, s, pdl);
+      if (p.d == 64) return launch_tc<64, true, 1>(pool_map, kblk_map, vblk_map, p, s, pdl);
+    }
+    return cudaErrorInvalidValue;
+  }
+  if (p.kv_terms == 2) return cudaErrorInvalidValue;
+  if (p.d == 128) return launch_tc<128, false, 1>(pool_map, kblk_map, vblk_map, p, s, pdl);
+  if (p.d == 64) return launch_tc<64, false, 1>(pool_map, kblk_map, vblk_map, p, s, pdl);
   return cudaErrorInvalidValue;
 }
+
+int attention_tc_target_split_pages() { return kTargetSplitPagesTc; }
 
 }  // namespace dflash

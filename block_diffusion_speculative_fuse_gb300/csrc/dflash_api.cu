@@ -351,15 +351,26 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
   const int rows = batch * n;
   const int H = c.hidden;
   const int max_keys = kv->max_pages * c.page_size;
-  // drafter attention on tcgen05: tensor maps over the pool and the block K/V
-  const int tc_pages = kv->max_pages + (n + 15) / 16;
-  const int tc_split_pages = attention_tc_split_pages(c.head_dim, batch * c.n_kv_heads, tc_pages);
-  const uint64_t pool_rows = static_cast<uint64_t>(c.n_layers) * kv->n_pages * 2 *
+  // attention on tcgen05: tensor maps over the pool and the block K/V.  The
+  // drafter: all block rows per CTA, key splits from an occupancy model.  The
+  // target (causal): query tiles of 64/G block rows and fixed 512-key splits,
+  // chosen per cache (never per call), so block verify and one-token decode
+  // run the same per-row arithmetic.
+  const int terms = kv_terms_of(c);
+  const int G = c.n_q_heads / c.n_kv_heads;
+  const int tc_pages = kv->max_pages + (m->is_draft ? (n + 15) / 16 : 0);
+  const int tc_split_pages = m->is_draft
+                                 ? attention_tc_split_pages(c.head_dim, batch * c.n_kv_heads, tc_pages)
+                                 : attention_tc_target_split_pages();
+  const int tc_splits = (tc_pages + tc_split_pages - 1) / tc_split_pages;
+  const int tc_rows_per_tile = m->is_draft ? n : std::max(1, 64 / G);
+  const uint64_t pool_rows = static_cast<uint64_t>(c.n_layers) * kv->n_pages * 2 * terms *
                              c.n_kv_heads * 16;
-  const bool use_tc = m->is_draft && m->attn_tc &&
-                      attention_tc_ok(c.head_dim, c.n_q_heads, c.n_kv_heads, n, c.page_size,
-                                      tc_split_pages) &&
-                      pool_rows + 16 < (1ull << 31);
+  const bool use_tc = m->attn_tc && pool_rows + 16 < (1ull << 31) &&
+                      (m->is_draft ? attention_tc_ok(c.head_dim, c.n_q_heads, c.n_kv_heads, n,
+                                                     c.page_size, tc_split_pages)
+                                   : ((c.head_dim == 64 || c.head_dim == 128) && G <= 64 &&
+                                      tc_splits <= kMaxAttnCluster));
   CUtensorMap pool_map, kblk_map, vblk_map;
   if (use_tc) {
     int rc = encode_map(&pool_map, kv->pool, pool_rows, c.head_dim, c.head_dim, 16);
@@ -415,10 +426,14 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       a.hq = c.n_q_heads;
       a.hkv = c.n_kv_heads;
       a.d = c.head_dim;
-      a.pool_row0 = static_cast<int>(static_cast<uint64_t>(l) * kv->n_pages * 2 * c.n_kv_heads * 16);
+      a.pool_row0 = static_cast<int>(static_cast<uint64_t>(l) * kv->n_pages * 2 * terms *
+                                     c.n_kv_heads * 16);
       a.pool_rows = static_cast<int>(pool_rows);
       a.split_pages = tc_split_pages;
-      a.n_splits = (tc_pages + tc_split_pages - 1) / tc_split_pages;
+      a.n_splits = tc_splits;
+      a.rows_per_tile = tc_rows_per_tile;
+      a.causal = m->is_draft ? 0 : 1;
+      a.kv_terms = terms;
       a.out = b.o;
       a.out_lo = b.o_lo;
       a.status = ws.status();
@@ -843,14 +858,15 @@ int dflash_lm_head_argmax(dflash_model m, const void* x, int32_t rows, int32_t* 
 int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t batch, int32_t B,
                          int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
                          int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
-                         const int32_t* anchor_pos_in, int32_t* anchor_pos_out, void* stream) {
+                         const int32_t* anchor_pos_in, int32_t* anchor_pos_out, int32_t* ctx_pos,
+                         void* stream) {
   if (target == nullptr || batch < 1 || B < 1 || B > 32 || (B > 1 && draft == nullptr))
     return DFLASH_ERR_INVALID_ARG;
   if ((tgt_len_out != nullptr && tgt_len_in == nullptr) ||
-      (anchor_pos_out != nullptr && anchor_pos_in == nullptr))
+      ((anchor_pos_out != nullptr || ctx_pos != nullptr) && anchor_pos_in == nullptr))
     return DFLASH_ERR_INVALID_ARG;
   DF_CUDA(verify_launch(draft, target, batch, B, out_tokens, n_accept, tgt_len_in, tgt_len_out,
-                        ctx_pending, anchor_out, anchor_pos_in, anchor_pos_out,
+                        ctx_pending, anchor_out, anchor_pos_in, anchor_pos_out, ctx_pos,
                         static_cast<cudaStream_t>(stream), true));
   return DFLASH_OK;
 }
@@ -865,15 +881,15 @@ int dflash_verify_sampling(const int32_t* draft, const float* draft_logits,
                            double temperature, const double* u, const double* w,
                            int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
                            int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
-                           const int32_t* anchor_pos_in, int32_t* anchor_pos_out, void* ws,
-                           size_t ws_bytes, void* stream) {
+                           const int32_t* anchor_pos_in, int32_t* anchor_pos_out, int32_t* ctx_pos,
+                           void* ws, size_t ws_bytes, void* stream) {
   if (target_logits == nullptr || w == nullptr || out_tokens == nullptr || batch < 1 || B < 1 ||
       B > 32 || vocab < 1 || !(temperature > 0.0) || !std::isfinite(temperature))
     return DFLASH_ERR_INVALID_ARG;
   if (B > 1 && (draft == nullptr || draft_logits == nullptr || u == nullptr))
     return DFLASH_ERR_INVALID_ARG;
   if ((tgt_len_out != nullptr && tgt_len_in == nullptr) ||
-      (anchor_pos_out != nullptr && anchor_pos_in == nullptr))
+      ((anchor_pos_out != nullptr || ctx_pos != nullptr) && anchor_pos_in == nullptr))
     return DFLASH_ERR_INVALID_ARG;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255)) return DFLASH_ERR_INVALID_ARG;
   if (ws_bytes < dflash_sampling_workspace_bytes(batch, B)) return DFLASH_ERR_CAPACITY;
@@ -881,7 +897,8 @@ int dflash_verify_sampling(const int32_t* draft, const float* draft_logits,
   DF_CUDA(verify_sampling_launch(draft, draft_logits, target_logits, batch, B, vocab, temperature,
                                  u, w, reinterpret_cast<double2*>(base + kHeaderBytes), out_tokens,
                                  n_accept, tgt_len_in, tgt_len_out, ctx_pending, anchor_out,
-                                 anchor_pos_in, anchor_pos_out, reinterpret_cast<int32_t*>(base),
+                                 anchor_pos_in, anchor_pos_out, ctx_pos,
+                                 reinterpret_cast<int32_t*>(base),
                                  static_cast<cudaStream_t>(stream), true));
   return DFLASH_OK;
 }

@@ -33,8 +33,9 @@ struct GemmCfg {
   // slots the next kernel's CTAs (programmatic dependent launch) occupy the
   // third and prefetch their first weight stages.  A split activation operand
   // (hi + lo tiles) enlarges a stage, so those variants keep fewer stages.
+  // (two-term BN = 128: 2 stages of 48 KB, so two CTAs fit per SM)
   static constexpr int STAGES =
-      SPLIT ? (BN <= 64 ? 3 : BN <= 128 ? 4 : 2)
+      SPLIT ? (BN <= 64 ? 3 : 2)
             : (BN <= 16 ? 4 : BN <= 32 ? 3 : BN <= 64 ? 4 : BN <= 128 ? 6 : 4);
   static constexpr int A_BYTES = kTileN * kTileK * 2;  // 16 KB
   static constexpr int B_BYTES = BN * kTileK * 2;      // one activation tile

@@ -162,6 +162,9 @@ struct AttnTcParams {
   int pool_rows;         // rows of the pool map (a row index that reads as zeros)
   int split_pages;       // 16-key pages per key split
   int n_splits;          // key splits = cluster size (<= kMaxAttnCluster)
+  int rows_per_tile;     // block rows per CTA (grid.z = query tiles); the drafter: n
+  int causal;            // 1: target pass (pool keys [0, pos0 + i] for row i; no block keys)
+  int kv_terms;          // 2: the pool pages hold K, V, K_lo, V_lo planes (causal only)
   uint16_t* out;         // [batch*n][hq][d]
   uint16_t* out_lo;      // optional low halves
   int32_t* status;
@@ -174,6 +177,8 @@ cudaError_t attention_tc_launch(const CUtensorMap* pool_map, const CUtensorMap* 
 int attention_tc_split_pages(int d, int pairs, int total_pages);
 // Occupancy queries behind attention_tc_split_pages (call outside capture).
 void attention_tc_prepare(int d);
+// Key pages per split of the causal (target) variant: fixed.
+int attention_tc_target_split_pages();
 bool attention_tc_ok(int d, int hq, int hkv, int n, int page_size, int split_pages);
 size_t attention_part_floats(int n_splits, int rows, int hq, int d);
 bool attention_cluster_ok(int d, int hq, int hkv, int n_splits);
@@ -198,8 +203,8 @@ cudaError_t argmax_reduce_launch(const float* val, const int32_t* idx, int rows,
 cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int batch, int B,
                           int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
                           int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
-                          const int32_t* anchor_pos_in, int32_t* anchor_pos_out, cudaStream_t s,
-                          bool pdl);
+                          const int32_t* anchor_pos_in, int32_t* anchor_pos_out, int32_t* ctx_pos,
+                          cudaStream_t s, bool pdl);
 cudaError_t synth_target_launch(const int32_t* draft, int batch, int B, const uint64_t* thr,
                                 int vocab, uint64_t seed, int64_t* step, int advance,
                                 int32_t* target, cudaStream_t s, bool pdl);
@@ -213,8 +218,8 @@ cudaError_t verify_sampling_launch(const int32_t* draft, const float* q_rows, co
                                    int32_t* n_accept, const int32_t* tgt_len_in,
                                    int32_t* tgt_len_out, int32_t* ctx_pending,
                                    int32_t* anchor_out, const int32_t* anchor_pos_in,
-                                   int32_t* anchor_pos_out, int32_t* status, cudaStream_t s,
-                                   bool pdl);
+                                   int32_t* anchor_pos_out, int32_t* ctx_pos, int32_t* status,
+                                   cudaStream_t s, bool pdl);
 cudaError_t sample_rows_launch(const float* rows, int n_used, int block, int skip, int V, double T,
                                const double* a, double2* stats, int32_t* out, cudaStream_t s,
                                bool pdl);

@@ -177,7 +177,8 @@ __global__ void __launch_bounds__(kSampThreads)
                            const double* w, int32_t* out_tokens, int32_t* n_accept,
                            const int32_t* tgt_len_in, int32_t* tgt_len_out, int32_t* ctx_pending,
                            int32_t* anchor_out, const int32_t* anchor_pos_in,
-                           int32_t* anchor_pos_out, int batch, int32_t* status) {
+                           int32_t* anchor_pos_out, int32_t* ctx_pos, int batch,
+                           int32_t* status) {
   __shared__ double red[72];
   __shared__ int found;
   __shared__ int s_n;
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(kSampThreads)
     const int j = threadIdx.x;
     if (j == n) out_tokens[static_cast<size_t>(r) * B + j] = tok;
     if (j > n) out_tokens[static_cast<size_t>(r) * B + j] = -1;
+    if (ctx_pos != nullptr) ctx_pos[static_cast<size_t>(r) * B + j] = j <= n ? anchor_pos_in[r] + j : -1;
   }
   if (threadIdx.x == 0) {
     if (n_accept != nullptr) n_accept[r] = n;
@@ -283,8 +285,8 @@ cudaError_t verify_sampling_launch(const int32_t* draft, const float* q_rows, co
                                    int32_t* n_accept, const int32_t* tgt_len_in,
                                    int32_t* tgt_len_out, int32_t* ctx_pending,
                                    int32_t* anchor_out, const int32_t* anchor_pos_in,
-                                   int32_t* anchor_pos_out, int32_t* status, cudaStream_t s,
-                                   bool pdl) {
+                                   int32_t* anchor_pos_out, int32_t* ctx_pos, int32_t* status,
+                                   cudaStream_t s, bool pdl) {
   int nq = batch * (B - 1), np = batch * B, one = 1;
   float Tf = static_cast<float>(T);
   void* a1[] = {&q_rows, &nq, &B, &one, &p_rows, &np, &V, &Tf, &stats};
@@ -292,7 +294,7 @@ cudaError_t verify_sampling_launch(const int32_t* draft, const float* q_rows, co
   if (e != cudaSuccess) return e;
   void* a2[] = {&draft, &q_rows, &p_rows, &B, &V, &Tf, &T, &stats, &u, &w, &out_tokens, &n_accept,
                 &tgt_len_in, &tgt_len_out, &ctx_pending, &anchor_out, &anchor_pos_in,
-                &anchor_pos_out, &batch, &status};
+                &anchor_pos_out, &ctx_pos, &batch, &status};
   return launch_k(reinterpret_cast<const void*>(verify_sampling_kernel), dim3(batch), a2, s, pdl);
 }
 

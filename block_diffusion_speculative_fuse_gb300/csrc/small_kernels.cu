@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(128)
     verify_kernel(const int32_t* draft, const int32_t* target, int batch, int B,
                   int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
                   int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
-                  const int32_t* anchor_pos_in, int32_t* anchor_pos_out) {
+                  const int32_t* anchor_pos_in, int32_t* anchor_pos_out, int32_t* ctx_pos) {
   griddep_launch_dependents();
   griddep_wait();
   const int r = blockIdx.x * 4 + threadIdx.x / 32;
@@ -269,10 +269,11 @@ __global__ void __launch_bounds__(128)
   const int n = mask ? __ffs(mask) - 1 : B - 1;
   const int bonus = __shfl_sync(0xffffffffu, t, n);
   const int tl = (lane == 0 && tgt_len_in != nullptr) ? tgt_len_in[r] : 0;
-  const int ap = (lane == 0 && anchor_pos_in != nullptr) ? anchor_pos_in[r] : 0;
+  const int ap = __shfl_sync(0xffffffffu, (lane == 0 && anchor_pos_in != nullptr) ? anchor_pos_in[r] : 0, 0);
   __syncwarp();
   if (lane < B && out_tokens != nullptr)
     out_tokens[static_cast<size_t>(r) * B + lane] = lane <= n ? t : -1;
+  if (lane < B && ctx_pos != nullptr) ctx_pos[static_cast<size_t>(r) * B + lane] = lane <= n ? ap + lane : -1;
   if (lane == 0) {
     if (n_accept != nullptr) n_accept[r] = n;
     if (tgt_len_out != nullptr) tgt_len_out[r] = tl + n + 1;
@@ -368,11 +369,11 @@ cudaError_t argmax_reduce_launch(const float* val, const int32_t* idx, int rows,
 cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int batch, int B,
                           int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
                           int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
-                          const int32_t* anchor_pos_in, int32_t* anchor_pos_out, cudaStream_t s,
-                          bool pdl) {
+                          const int32_t* anchor_pos_in, int32_t* anchor_pos_out, int32_t* ctx_pos,
+                          cudaStream_t s, bool pdl) {
   return launch(verify_kernel, dim3((batch + 3) / 4), dim3(128), 0, s, pdl, draft, target, batch,
                 B, out_tokens, n_accept, tgt_len_in, tgt_len_out, ctx_pending, anchor_out,
-                anchor_pos_in, anchor_pos_out);
+                anchor_pos_in, anchor_pos_out, ctx_pos);
 }
 cudaError_t synth_target_launch(const int32_t* draft, int batch, int B, const uint64_t* thr,
                                 int vocab, uint64_t seed, int64_t* step, int advance,

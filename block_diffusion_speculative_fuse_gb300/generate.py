@@ -9,10 +9,15 @@ Speculative iteration (lossless at temperature 0):
      L..L+B-1, writing its K/V and tapping hidden states;
   3. dflash_verify_greedy accepts n, emits t_1..t_{n+1}, advances lengths;
   4. dflash_ctx_fuse turns the tapped states of the B rows into context rows;
-     only rows 0..n become pending rows for the next draft (others get
-     position -1 and are skipped).
-The target cache needs no explicit rollback: positions past L+n are
-rewritten before any row at or after them attends to them.
+     only rows 0..n become pending rows for the next draft (the verify
+     kernel writes their positions; the others get -1 and are skipped).
+The loop state (anchors, positions, pending rows, emitted counts, emitted
+tokens) stays on the device; each iteration reads back only the emitted
+count per request (batch int32) for the stop test.  The target cache needs
+no explicit rollback: positions past L+n are rewritten before any row at or
+after them attends to them.  Fusing only the accepted rows would not save
+weight bytes: the fuse GEMM streams its weights once for any row count up to
+a few hundred.
 """
 import numpy as np
 import torch
@@ -111,38 +116,47 @@ class SpecDecoder:
         req = i32(np.repeat(np.arange(b), P), dev)
         pos = i32(np.tile(np.arange(P), b), dev)
         B.dflash_kv_append(self.drafter.handle, ctx, req, pos, b * P, self.dkv.struct, self.ws_d)
-        L = np.full(b, P, dtype=np.int64)
-        result = [[int(t)] for t in anchor.cpu().numpy()]
+        first = anchor.clone()
+        max_iters = n_tokens  # at least one token per request per iteration
+        history = torch.full((max_iters, b, Bk), -1, dtype=torch.int32, device=dev)
         draft = torch.zeros((b, max(1, Bk - 1)), dtype=torch.int32, device=dev)
-        out_tok = torch.zeros((b, Bk), dtype=torch.int32, device=dev)
         n_acc = torch.zeros(b, dtype=torch.int32, device=dev)
-        anchor_pos = i32(L, dev)
-        anchor_pos_out = torch.zeros(b, dtype=torch.int32, device=dev)
-        anchor_out = torch.zeros(b, dtype=torch.int32, device=dev)
+        emitted = torch.ones(b, dtype=torch.int32, device=dev)  # the prefill's token
+        anchor_pos = torch.full((b,), P, dtype=torch.int32, device=dev)
+        anchor_pos_next = torch.zeros(b, dtype=torch.int32, device=dev)
+        anchor_next = torch.zeros(b, dtype=torch.int32, device=dev)
         pend_ctx = torch.empty((b * Bk, d.hidden), dtype=torch.bfloat16, device=dev)
         pend_req = i32(np.repeat(np.arange(b), Bk), dev)
+        pend_pos = torch.full((b, Bk), -1, dtype=torch.int32, device=dev)
+        rows = torch.empty((b, Bk), dtype=torch.int32, device=dev)
+        counts = torch.empty(b, dtype=torch.int32, device="cpu").pin_memory()
         T = 0
-        pend_pos = None
-        while min(len(r) for r in result) < n_tokens:
+        it = 0
+        while it < max_iters:
             B.dflash_draft_block(self.drafter.handle, anchor, anchor_pos, b, self.dkv.struct,
                                  pend_ctx if T else None, pend_req if T else None,
                                  pend_pos if T else None, T, draft, None, None, self.ws_d)
-            rows = torch.cat([anchor.view(b, 1), draft[:, :Bk - 1]], dim=1).contiguous()
+            rows[:, 0] = anchor
+            if Bk > 1:
+                rows[:, 1:] = draft[:, :Bk - 1]
             t, taps = self.target.forward(rows, anchor_pos, Bk, want_taps=True)
-            B.dflash_verify_greedy(draft if Bk > 1 else None, t, b, Bk, out_tok, n_acc, None,
-                                   None, None, anchor_out, anchor_pos, anchor_pos_out)
+            B.dflash_verify_greedy(draft if Bk > 1 else None, t, b, Bk, history[it], n_acc,
+                                   emitted, emitted, None, anchor_next, anchor_pos,
+                                   anchor_pos_next, ctx_pos=pend_pos)
             B.dflash_ctx_fuse(self.drafter.handle, taps, b * Bk, pend_ctx, self.ws_d)
-            n_np = n_acc.cpu().numpy()
-            toks = out_tok.cpu().numpy()
-            self.stats.extend(int(x) for x in n_np)
-            pp = np.full((b, Bk), -1, dtype=np.int32)
-            for r in range(b):
-                k = int(n_np[r]) + 1
-                result[r].extend(int(x) for x in toks[r, :k])
-                pp[r, :k] = L[r] + np.arange(k)
-                L[r] += k
-            pend_pos = i32(pp.reshape(-1), dev)
             T = b * Bk
-            anchor = anchor_out.clone()
-            anchor_pos = anchor_pos_out.clone()
-        return np.array([r[:n_tokens] for r in result], dtype=np.int32)
+            anchor, anchor_next = anchor_next, anchor
+            anchor_pos, anchor_pos_next = anchor_pos_next, anchor_pos
+            it += 1
+            counts.copy_(emitted)  # the stop test: one D2H of batch int32
+            if int(counts.min()) >= n_tokens:
+                break
+        hist = history[:it].cpu().numpy()
+        first = first.cpu().numpy()
+        result = []
+        for r in range(b):
+            em = hist[:, r, :]
+            toks = [int(first[r])] + [int(x) for x in em[em >= 0]]
+            self.stats.extend(int((row >= 0).sum()) - 1 for row in em)
+            result.append(toks[:n_tokens])
+        return np.array(result, dtype=np.int32)

@@ -234,13 +234,18 @@ int dflash_lm_head_argmax(dflash_model m, const void* x, int32_t rows, int32_t* 
  * n = longest prefix with draft == target (0..B-1).  Outputs:
  *   out_tokens [batch][B]: t_1..t_{n+1}, then -1;   n_accept [batch];
  *   tgt_len_out = tgt_len_in + n + 1;  ctx_pending = n + 1;
- *   anchor_out = t_{n+1};  anchor_pos_out = anchor_pos_in + n + 1.
- * Any output may be NULL (not written); tgt_len_out and anchor_pos_out need
- * their inputs.  In/out pairs may alias.  Pure integer work, bit-exact. */
+ *   anchor_out = t_{n+1};  anchor_pos_out = anchor_pos_in + n + 1;
+ *   ctx_pos [batch][B]: the positions of the block rows that become draft
+ *   context (anchor and accepted drafts), anchor_pos_in + j for j <= n, then
+ *   -1: the pending rows' positions for the next dflash_draft_block.
+ * Any output may be NULL (not written); tgt_len_out, anchor_pos_out and
+ * ctx_pos need their inputs.  In/out pairs may alias (ctx_pos must not alias
+ * anchor_pos_in).  Pure integer work, bit-exact. */
 int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t batch, int32_t B,
                          int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
                          int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
-                         const int32_t* anchor_pos_in, int32_t* anchor_pos_out, void* stream);
+                         const int32_t* anchor_pos_in, int32_t* anchor_pos_out, int32_t* ctx_pos,
+                         void* stream);
 
 /* Verification at temperature T > 0 ("DFlash: how block diffusion boosts
  * NVIDIA Blackwell throughput", section "Real-world integration": sampling-
@@ -273,8 +278,8 @@ int dflash_verify_sampling(const int32_t* draft, const float* draft_logits,
                            double temperature, const double* u, const double* w,
                            int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,
                            int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
-                           const int32_t* anchor_pos_in, int32_t* anchor_pos_out, void* ws,
-                           size_t ws_bytes, void* stream);
+                           const int32_t* anchor_pos_in, int32_t* anchor_pos_out, int32_t* ctx_pos,
+                           void* ws, size_t ws_bytes, void* stream);
 
 /* Draft sampling for the temperature-T verify: one categorical draw from
  * softmax(z / T) per used row of logits fp32 [n_blocks][block][vocab] (with

@@ -306,7 +306,9 @@ def verify_greedy(draft, target):
 def verify_batch(draft, target, tgt_len, anchor_pos):
     """Batched form with the bookkeeping the hot path needs: out_tokens
     [b][B] (-1 padded), n [b], new target length, pending context rows n+1,
-    new anchor token and position."""
+    their positions ctx_pos [b][B] (the anchor's and the accepted drafts':
+    anchor_pos + j for j <= n, then -1; the rows spec_generate appends to
+    the draft context), new anchor token and position."""
     draft = np.asarray(draft)
     target = np.asarray(target)
     b, B = target.shape
@@ -319,9 +321,12 @@ def verify_batch(draft, target, tgt_len, anchor_pos):
     tgt_len = np.asarray(tgt_len, dtype=np.int64)
     anchor_pos = np.asarray(anchor_pos, dtype=np.int64)
     new_anchor = target[np.arange(b), n]
+    j = np.arange(B)[None, :]
+    ctx_pos = np.where(j <= n[:, None], anchor_pos[:, None] + j, -1)
     return dict(out_tokens=out, n_accept=n,
                 tgt_len=(tgt_len + n + 1).astype(np.int32),
                 ctx_pending=(n + 1).astype(np.int32),
+                ctx_pos=ctx_pos.astype(np.int32),
                 anchor=new_anchor.astype(np.int32),
                 anchor_pos=(anchor_pos + n + 1).astype(np.int32))
 

@@ -71,13 +71,17 @@ def test_model_create_rejects_bad_args(lib):
 def test_verify_rejects_bad_sizes(lib):
     f = lib.dflash_verify_greedy
     dummy = ctypes.c_void_p(0x1000)
-    assert f(dummy, dummy, 0, 16, *([None] * 8), None) == -1      # batch 0
-    assert f(dummy, dummy, 1, 0, *([None] * 8), None) == -1       # B 0
-    assert f(dummy, dummy, 1, 33, *([None] * 8), None) == -1      # B > 32
-    assert f(None, dummy, 1, 4, *([None] * 8), None) == -1        # drafts missing
+    assert f(dummy, dummy, 0, 16, *([None] * 9), None) == -1      # batch 0
+    assert f(dummy, dummy, 1, 0, *([None] * 9), None) == -1       # B 0
+    assert f(dummy, dummy, 1, 33, *([None] * 9), None) == -1      # B > 32
+    assert f(None, dummy, 1, 4, *([None] * 9), None) == -1        # drafts missing
     # an output length without its input
-    args = [None] * 8
+    args = [None] * 9
     args[3] = dummy
+    assert f(dummy, dummy, 1, 4, *args, None) == -1
+    # pending positions without the anchor positions they are built from
+    args = [None] * 9
+    args[8] = dummy
     assert f(dummy, dummy, 1, 4, *args, None) == -1
 
 
@@ -122,7 +126,7 @@ def test_sampling_calls_reject_bad_args_before_launch(lib):
     assert need == 64 * 1024 + ((2 * 31 * 16 + 255) // 256) * 256
     assert lib.dflash_sampling_workspace_bytes(0, 16) == 0
     f = lib.dflash_verify_sampling
-    ok = [d, d, d, 2, 16, 1000, 0.7, d, d] + [d] + [None] * 7
+    ok = [d, d, d, 2, 16, 1000, 0.7, d, d] + [d] + [None] * 8
     assert f(*ok[:6], 0.0, *ok[7:], ws, need, None) == -1          # T = 0
     assert f(*ok[:6], float("nan"), *ok[7:], ws, need, None) == -1
     assert f(*ok[:3], 2, 33, *ok[5:], ws, need, None) == -1        # B > 32

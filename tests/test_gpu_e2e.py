@@ -152,3 +152,35 @@ def test_target_forward_rows_independent_of_batch():
         torch.cuda.synchronize()
         assert torch.equal(l1, l3[r * n:(r + 1) * n]), r
         assert torch.equal(out1[0], out3[r])
+
+
+@pytest.mark.parametrize("attn_tc", ["0", "1"])
+def test_spec_equals_ar_either_target_attention(attn_tc, monkeypatch):
+    """Both target attention kernels (tcgen05 query tiles with fixed key
+    splits, and the mma.sync fallback; chosen at model creation) keep the
+    target batch invariant: speculative == autoregressive, and one block
+    verify gives the logits of one-token decode bit for bit."""
+    from block_diffusion_speculative_fuse_gb300.device import i32
+    from block_diffusion_speculative_fuse_gb300.generate import SpecDecoder, TargetRunner, \
+        ar_generate
+    monkeypatch.setenv("DFLASH_ATTN_TC", attn_tc)
+    wl = W.get_workload("tiny_e2e")
+    shared, tw, dw, tm, dm = models(wl, target_std=0.05)
+    prompt = W.uniform_tokens(2 * 40, wl.target.vocab, 8, 8).reshape(2, 40)
+    ar = ar_generate(TargetRunner(tm, 2, 40 + 48 + 1, 40), prompt, 48)
+    sd = SpecDecoder(tm, dm, wl.tap_layers, 2, 40 + 48)
+    assert np.array_equal(sd.generate(prompt, 48), ar)
+    # 8 rows at once vs one at a time, after a 40-token prefill
+    V, n = wl.target.vocab, 8
+    toks = W.uniform_tokens(n, V, 9, 9)
+    blk = TargetRunner(tm, 1, 64, 40)
+    blk.forward(i32(prompt[:1]), i32([0]), 40)
+    lb = torch.zeros((n, V), dtype=torch.float32, device="cuda")
+    blk.forward(i32(toks[None]), i32([40]), n, logits=lb)
+    one = TargetRunner(tm, 1, 64, 40)
+    one.forward(i32(prompt[:1]), i32([0]), 40)
+    for i in range(n):
+        l1 = torch.zeros((1, V), dtype=torch.float32, device="cuda")
+        one.forward(i32(toks[None, i:i + 1]), i32([40 + i]), 1, logits=l1)
+        torch.cuda.synchronize()
+        assert torch.equal(l1[0], lb[i]), i

@@ -62,8 +62,9 @@ def test_verify_bitexact_random_and_all_n():
         out = torch.full((n_req, Bs), 7, dtype=torch.int32, device="cuda")
         n = torch.zeros(n_req, dtype=torch.int32, device="cuda")
         tlo, cp, ao, apo = (torch.zeros(n_req, dtype=torch.int32, device="cuda") for _ in range(4))
+        cpos = torch.full((n_req, Bs), 7, dtype=torch.int32, device="cuda")
         B.dflash_verify_greedy(d_d if Bs > 1 else None, d_t, n_req, Bs, out, n, d_tl, tlo, cp,
-                               ao, d_ap, apo)
+                               ao, d_ap, apo, ctx_pos=cpos)
         torch.cuda.synchronize()
         ref = O.verify_batch(draft[:, :Bs - 1], target, tl, ap)
         assert np.array_equal(n.cpu().numpy(), ref["n_accept"])
@@ -72,6 +73,7 @@ def test_verify_bitexact_random_and_all_n():
         assert np.array_equal(cp.cpu().numpy(), ref["ctx_pending"])
         assert np.array_equal(ao.cpu().numpy(), ref["anchor"])
         assert np.array_equal(apo.cpu().numpy(), ref["anchor_pos"])
+        assert np.array_equal(cpos.cpu().numpy(), ref["ctx_pos"])
         assert set(np.unique(ref["n_accept"])) == set(range(Bs))
 
 

@@ -206,6 +206,8 @@ def test_verify_batch_bookkeeping():
     assert r["ctx_pending"].tolist() == [3, 4]
     assert r["anchor"].tolist() == [2, 8]
     assert r["anchor_pos"].tolist() == [103, 54]
+    # the anchor (position 100 / 50) and the accepted drafts become context
+    assert r["ctx_pos"].tolist() == [[100, 101, 102, -1], [50, 51, 52, 53]]
 
 
 def test_synthetic_acceptance_closed_form():
