@@ -18,7 +18,9 @@ the even mantissa, and saturates finite values beyond 448 to +-448.
 Reading: the scale of a (position, head) vector of d values is amax / 448,
 so its largest element maps to the top code (an all-zero vector keeps scale
 1).  The pages name no scaling granularity; per (position, head) is the
-plainest choice that needs no calibration data.
+plainest choice that needs no calibration data.  Nor do they fix the
+precision of value / scale: the quotient is taken in fp32, the precision a
+GPU kernel forms it in, so that both decide each code from the same number.
 """
 import numpy as np
 
@@ -63,11 +65,20 @@ def e4m3_encode(x):
 
 def quantize_kv(x):
     """x: [..., d] K or V vectors.  Returns (codes uint8 [..., d], scale
-    fp32 [...]) with scale = amax / 448 per vector (1 for a zero vector)."""
+    fp32 [...]) with scale = amax / 448 per vector (1 for a zero vector).
+
+    The code is decided from the quotient value / scale formed in fp32 (the
+    values and the scale are fp32 numbers; the division is rounded to
+    nearest), then rounded to E4M3.  With bf16 inputs 448 * value / amax is
+    often exactly halfway between two codes, and the rounded fp32 scale moves
+    the exact quotient just off that midpoint in either direction; deciding
+    from the fp32 quotient makes every such case a tie, resolved to the even
+    mantissa."""
     x = np.asarray(x, dtype=F64)
     amax = np.max(np.abs(x), axis=-1)
     scale = np.where(amax > 0, amax / E4M3_MAX, 1.0).astype(np.float32)
-    codes = e4m3_encode(x / scale.astype(F64)[..., None])
+    q = np.asarray(x, dtype=np.float32) / scale[..., None]
+    codes = e4m3_encode(q.astype(F64))
     return codes, scale
 
 

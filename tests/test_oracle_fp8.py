@@ -56,6 +56,31 @@ def test_ties_go_to_the_even_mantissa_and_large_values_saturate():
     assert enc(np.nan) == 0x7F
 
 
+def test_quantize_kv_matches_torch_fp32_quotient_and_cast():
+    """quantize_kv on bf16 vectors against PyTorch: fp32 scale amax/448,
+    fp32 division, float8_e4m3fn cast (round to nearest even).  Vectors of
+    small integers times a power of two make 448 * value / amax land exactly
+    on E4M3 midpoints often, where an fp64 quotient would decide otherwise."""
+    g = np.random.default_rng(3)
+    ints = g.integers(-255, 256, size=(4000, 64)).astype(np.float64)
+    ints[:, 0] = g.choice([255.0, 224.0, 192.0, 160.0, 96.0, 7.0], size=4000)
+    x = ints * np.exp2(g.integers(-20, 10, size=(4000, 1)))
+    x = np.concatenate([x, g.normal(size=(4000, 64)) * np.exp2(g.uniform(-20, 10, (4000, 1)))])
+    x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()  # bf16 values
+    codes, scale = F.quantize_kv(x)
+    xt = torch.from_numpy(x).to(torch.float32)
+    amax = xt.abs().amax(-1)
+    st = torch.where(amax > 0, (amax.double() / 448.0).float(), torch.ones_like(amax))
+    assert np.array_equal(scale, st.numpy())
+    q = xt / st[:, None]
+    assert float(q.abs().max()) < 464.0            # inside torch's finite range
+    ref = q.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+    # the exact quotient decides differently from the fp32 one in many places
+    exact = F.e4m3_encode(x / scale.astype(np.float64)[:, None])
+    assert int((exact != codes).sum()) > 100
+
+
 def test_kv_scaling_error_bound():
     """Per (position, head) scale amax/448: every element is within half a
     3-bit-mantissa step of its value (relative 2^-4) or, below the normal
