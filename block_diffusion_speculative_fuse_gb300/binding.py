@@ -47,7 +47,8 @@ class DflashWeights(ctypes.Structure):
 class DflashKV(ctypes.Structure):
     _fields_ = [("pool", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
                 ("n_pages", ctypes.c_int32), ("max_pages", ctypes.c_int32),
-                ("n_rows", ctypes.c_int32)]
+                ("n_rows", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("scales", ctypes.c_void_p)]
 
 
 EXPORTS = {
@@ -83,6 +84,8 @@ EXPORTS = {
     "dflash_verify_greedy": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                             ctypes.c_int32] + [ctypes.c_void_p] * 9 +
                              [ctypes.c_void_p]),
+    "dflash_kv_quantize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p]),
     "dflash_sampling_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32]),
     "dflash_verify_sampling": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -220,6 +223,11 @@ def dflash_draft_block(h, anchor, anchor_pos, batch, kv: DflashKV, pending_ctx, 
         h, ptr(anchor), ptr(anchor_pos), batch, ctypes.byref(kv), ptr(pending_ctx),
         ptr(pending_req), ptr(pending_pos), T, ptr(draft), ptr(logits), ptr(hidden), ptr(ws),
         ws.numel() * ws.element_size(), stream_handle(stream)))
+
+
+def dflash_kv_quantize(h, src: DflashKV, dst: DflashKV, stream=None):
+    return _check("dflash_kv_quantize", load().dflash_kv_quantize(
+        h, ctypes.byref(src), ctypes.byref(dst), stream_handle(stream)))
 
 
 def dflash_sampling_workspace_bytes(batch, B):

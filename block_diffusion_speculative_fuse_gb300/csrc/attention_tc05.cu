@@ -49,9 +49,17 @@ constexpr int kThreads = 192;      // warps 0-3 softmax, 4 TMA, 5 MMA
 
 // TERMS = 2: every key chunk also carries the low bf16 terms of K and V
 // (planes K, V, K_lo, V_lo in a stage, as in the pool's pages).
-template <int D, int TERMS = 1>
+// FP8: the context pages hold E4M3 codes and per-vector scales; they arrive
+// in a ring of code stages and two converter warps turn them into the bf16
+// stages the MMAs read (block keys arrive there as bf16 directly).
+template <int D, int TERMS = 1, bool FP8 = false>
 struct TcCfg {
-  static constexpr int STAGES = TERMS == 2 ? 2 : 4;
+  static constexpr int THREADS = FP8 ? 256 : 192;  // + warps 6-7: converters
+  static constexpr int STAGES = (TERMS == 2 || FP8) ? 2 : 4;
+  static constexpr int F8_STAGES = FP8 ? 4 : 0;
+  static constexpr int K8_BYTES = kChunkKeys * D;               // [64 keys][D] codes
+  static constexpr int F8_STAGE_BYTES = 2 * K8_BYTES;           // K codes then V codes
+  static constexpr int SC_BYTES = 2 * kChunkKeys * 4;           // K scales then V scales
   static constexpr int PLANES = 2 * TERMS;
   static constexpr int HALVES = D / 64;
   static constexpr int Q_BYTES = 128 * D * 2;                   // [HALVES][128 rows][64]
@@ -63,14 +71,18 @@ struct TcCfg {
   static constexpr int Q_OFF = 0;
   static constexpr int P_OFF = Q_OFF + Q_BYTES;
   static constexpr int KV_OFF = P_OFF + 2 * P_BYTES;
-  static constexpr int PG_OFF = KV_OFF + STAGES * STAGE_BYTES;
+  static constexpr int F8_OFF = KV_OFF + STAGES * STAGE_BYTES;       // code ring
+  static constexpr int SC8_OFF = F8_OFF + F8_STAGES * F8_STAGE_BYTES;  // scales of the code ring
+  static constexpr int SCB_OFF = SC8_OFF + F8_STAGES * SC_BYTES;      // scales of the bf16 stages
+  static constexpr int PG_OFF = SCB_OFF + (FP8 ? STAGES * SC_BYTES : 0);
   static constexpr int PN_OFF = PG_OFF + kMaxPagesTc * 4;
   static constexpr int BAR_OFF = PN_OFF + kMaxPagesTc * 4;
   static constexpr int SMEM = BAR_OFF + 512 + 1024;             // barriers + alignment slack
   // combine staging (after the key loop, in the K/V stage area): 128 row slots
   // merge staging: at most 160 partial rows (rows per CTA x parts x splits
   // <= (R + splits) x parts) of D + 4 floats plus (m, l)
-  static_assert(160 * ((D + 4) * 4 + 8) <= STAGES * STAGE_BYTES, "merge staging must fit");
+  static_assert(160 * ((D + 4) * 4 + 8) <= STAGES * STAGE_BYTES + F8_STAGES * F8_STAGE_BYTES,
+                "merge staging must fit");
   static_assert(BOXES <= 32, "one TMA box per producer lane");
   static constexpr uint32_t TMEM_COLS = 256;                    // S0 | S1 | O
   static constexpr uint32_t S_COL0 = 0, O_COL = 128;
@@ -95,14 +107,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // separate block keys.  The CTA takes block rows [qt*rpt, (qt+1)*rpt) of its
 // request (p.rows_per_tile), so a row's arithmetic never depends on how many
 // rows the call has.
-template <int D, bool CAUSAL = false, int TERMS = 1>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool CAUSAL = false, int TERMS = 1, bool FP8 = false>
+__global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
     attn_tc05_kernel(const __grid_constant__ CUtensorMap pool_map,
                      const __grid_constant__ CUtensorMap kblk_map,
                      const __grid_constant__ CUtensorMap vblk_map,
                      const __grid_constant__ AttnTcParams p) {
-  using C = TcCfg<D, TERMS>;
+  using C = TcCfg<D, TERMS, FP8>;
+  static_assert(!FP8 || (!CAUSAL && TERMS == 1), "E4M3 context caches: drafter, one term");
   constexpr int kStages = C::STAGES;
+  constexpr int kThreads = C::THREADS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -114,6 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pv_done = p_full + 2;         // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pv_done + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* f8_full = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF + 256);  // FP8: code ring
+  uint64_t* f8_empty = f8_full + 4;
   int* pages_s = reinterpret_cast<int*>(sm + C::PG_OFF);   // pool page, -1 none, <= -2 block page
   int* pages_n = reinterpret_cast<int*>(sm + C::PN_OFF);   // valid keys of each staged page
 
@@ -129,8 +145,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
+      // FP8: a bf16 stage is complete when both converter warps have arrived
+      // (and the bf16 block keys they requested have landed)
+      mbar_init(&kv_full[s], FP8 ? 2 : 1);
       mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < C::F8_STAGES; ++s) {
+      mbar_init(&f8_full[s], 1);
+      mbar_init(&f8_empty[s], 2);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -227,7 +249,130 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (FP8 && warp == 4) {
+    // ------------------------------------------------ E4M3 producer: codes (TMA) and
+    // scales (bulk copies) of the context pages into the code ring
+    const uint64_t pol = l2_policy_evict_first();
+    constexpr int S8 = C::F8_STAGES > 0 ? C::F8_STAGES : 1;
+    int issued = 0;
+    for (int c = 0; c < nch; ++c) {
+      const int st = c % S8;
+      int n8 = 0;
+#pragma unroll
+      for (int pp = 0; pp < kChunkPages; ++pp) n8 += pages_s[c * kChunkPages + pp] >= 0 ? 1 : 0;
+      int ok = 1;
+      if (lane == 0) {
+        if (c >= S8 && !mbar_wait(&f8_empty[st], ((c / S8) & 1) ^ 1, abort_flag)) {
+          *abort_flag = 1;
+          raise_status(p.status, DFLASH_ERR_TIMEOUT, 315);
+          ok = 0;
+        } else {
+          mbar_arrive_expect_tx(&f8_full[st], n8 * 2 * (16 * D + 64));
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane < kChunkPages * 4) {
+        // lane -> (page, K|V, codes|scales)
+        const int pp = lane / 4, kv = (lane / 2) % 2, what = lane % 2;
+        const int id = pages_s[c * kChunkPages + pp];
+        if (id >= 0) {
+          const int row = p.pool_row0 + ((id * 2 + kv) * p.hkv + g) * 16;  // first vector of the page
+          if (what == 0)
+            tma_load_2d(sm + C::F8_OFF + st * C::F8_STAGE_BYTES + kv * C::K8_BYTES + pp * 16 * D,
+                        &pool_map, 0, row, &f8_full[st], pol);
+          else
+            bulk_load(sm + C::SC8_OFF + st * C::SC_BYTES + kv * (kChunkKeys * 4) + pp * 64,
+                      p.scales + row, 64, &f8_full[st]);
+        }
+      }
+      ++issued;
+      if (c == min(nch, S8) - 1) griddep_launch_dependents();
+    }
+    if (nch == 0 || issued < min(nch, S8)) griddep_launch_dependents();  // none issued, or an abort
+    if (lane == 0)
+      for (int c = max(0, issued - S8); c < issued; ++c)
+        mbar_wait(&f8_full[c % S8], (c / S8) & 1, nullptr);
+  } else if (FP8 && warp >= 6) {
+    // ------------------------------------------------ converters: code stage ->
+    // bf16 stage (exact values; invalid keys as zeros), per-key scales, and
+    // the bf16 block keys by TMA (first lane)
+    constexpr int S8 = C::F8_STAGES > 0 ? C::F8_STAGES : 1;
+    const uint64_t pol = l2_policy_evict_first();
+    const int t = tid - 192;
+    int done_c = 0;
+    for (int c = 0; c < nch; ++c) {
+      const int st8 = c % S8, sb = c % kStages;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&f8_full[st8], (c / S8) & 1, abort_flag));
+      if (ok && c >= kStages)
+        ok = __all_sync(0xffffffffu, mbar_wait(&kv_empty[sb], ((c / kStages) & 1) ^ 1, abort_flag));
+      if (!ok) {
+        *abort_flag = 1;
+        if (lane == 0) raise_status(p.status, DFLASH_ERR_TIMEOUT, 316);
+        break;
+      }
+      if (t == 0) {
+        int nb = 0;
+#pragma unroll
+        for (int pp = 0; pp < kChunkPages; ++pp) nb += pages_s[c * kChunkPages + pp] <= -2 ? 1 : 0;
+        if (nb > 0) {
+          mbar_expect_tx(&kv_full[sb], nb * 2 * C::HALVES * (16 * 64 * 2));
+          for (int pp = 0; pp < kChunkPages; ++pp) {
+            const int id = pages_s[c * kChunkPages + pp];
+            if (id > -2) continue;
+            const int y = (req * p.hkv + g) * p.n + (-2 - id) * 16;
+            for (int kv = 0; kv < 2; ++kv)
+              for (int hf = 0; hf < C::HALVES; ++hf)
+                tma_load_2d(sm + C::KV_OFF + sb * C::STAGE_BYTES + kv * C::K_BYTES + hf * C::KV_HALF +
+                                pp * 16 * 128,
+                            kv ? &vblk_map : &kblk_map, hf * 64, y, &kv_full[sb], pol);
+          }
+        }
+      }
+      const uint8_t* f8 = sm + C::F8_OFF + st8 * C::F8_STAGE_BYTES;
+      uint8_t* b16 = sm + C::KV_OFF + sb * C::STAGE_BYTES;
+      constexpr int CH = D / 8;  // 8-value pieces per key row
+      for (int idx = t; idx < kChunkPages * 2 * 16 * CH; idx += 64) {
+        const int c16 = idx % CH, rest = idx / CH;
+        const int key = rest % 16, kv = (rest / 16) % 2, pp = rest / 32;
+        const int id = pages_s[c * kChunkPages + pp];
+        if (id <= -2) continue;  // block keys arrive as bf16
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (id >= 0 && key < pages_n[c * kChunkPages + pp]) {
+          const uint2 cd = *reinterpret_cast<const uint2*>(f8 + kv * C::K8_BYTES + (pp * 16 + key) * D + c16 * 8);
+          o.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(cd.x & 0xFFFFu));
+          o.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(cd.x >> 16));
+          o.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(cd.y & 0xFFFFu));
+          o.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(cd.y >> 16));
+        }
+        *reinterpret_cast<uint4*>(b16 + kv * C::K_BYTES + (c16 / 8) * C::KV_HALF +
+                                  swz128(pp * 16 + key, c16 % 8)) = o;
+      }
+      float* scb = reinterpret_cast<float*>(sm + C::SCB_OFF + sb * C::SC_BYTES);
+      const float* sc8 = reinterpret_cast<const float*>(sm + C::SC8_OFF + st8 * C::SC_BYTES);
+      for (int k = t; k < 2 * kChunkKeys; k += 64) {
+        const int key = k % kChunkKeys, pp = key / 16;
+        const int id = pages_s[c * kChunkPages + pp];
+        float v = 0.f;
+        if (id <= -2)
+          v = 1.f;
+        else if (id >= 0 && (key % 16) < pages_n[c * kChunkPages + pp])
+          v = sc8[k];
+        scb[k] = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&f8_empty[st8]);
+        mbar_arrive(&kv_full[sb]);
+      }
+      done_c = c + 1;
+    }
+    // block-key copies still in flight after an abort land before the CTA exits
+    if (t == 0)
+      for (int c = max(0, done_c - kStages); c < done_c; ++c)
+        mbar_wait(&kv_full[c % kStages], (c / kStages) & 1, nullptr);
+  } else if (warp == 4) {
     // ------------------------------------------------ TMA producer (one box per lane)
     const uint64_t pol = l2_policy_evict_first();
     int issued = 0;
@@ -372,6 +517,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         s[j] = __uint_as_float(sr0[j]);
         s[32 + j] = __uint_as_float(sr1[j]);
       }
+      const float* sv = nullptr;  // FP8: the V scale of every key, folded into P
+      if constexpr (FP8) {
+        // K scales folded into the scores (S = scale_k * (q . codes))
+        const float* sk = reinterpret_cast<const float*>(sm + C::SCB_OFF + st * C::SC_BYTES);
+        sv = sk + kChunkKeys;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) s[j] *= sk[j];
+      }
       if (!full) {
         // invalid keys (stale or zero-filled rows) never contribute
 #pragma unroll
@@ -429,7 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 32; ++j) {
         const float p0 = ex2_approx(fmaf(s[2 * j], sl2, neg));
         const float p1 = ex2_approx(fmaf(s[2 * j + 1], sl2, neg));
-        pk[j] = pack_bf16x2(p0, p1);
+        if constexpr (FP8)
+          pk[j] = pack_bf16x2(p0 * sv[2 * j], p1 * sv[2 * j + 1]);  // P * scale_v
+        else
+          pk[j] = pack_bf16x2(p0, p1);
         ls4[j & 3] += p0 + p1;
       }
       l_sum += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
@@ -444,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c16 = 0; c16 < 8; ++c16)
         *reinterpret_cast<uint4*>(pbuf + swz128(prow, c16)) =
             make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-      if (stale) {
+      if (!FP8 && stale) {
         // rows past a context page's valid keys hold stale pool data: zero
         // their V rows (and low terms) so that 0 * V stays 0
         uint8_t* vst = sm + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
@@ -620,19 +776,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D, bool CAUSAL, int TERMS>
+template <int D, bool CAUSAL, int TERMS, bool FP8 = false>
 cudaError_t launch_tc(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
                       const CUtensorMap* vblk_map, const AttnTcParams& p, cudaStream_t s,
                       bool pdl) {
+  using C = TcCfg<D, TERMS, FP8>;
   static thread_local int attr_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc05_kernel<D, CAUSAL, TERMS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TcCfg<D, TERMS>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc05_kernel<D, CAUSAL, TERMS, FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_tc05_kernel<D, CAUSAL, TERMS>,
+    e = cudaFuncSetAttribute(attn_tc05_kernel<D, CAUSAL, TERMS, FP8>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_device = dev;
@@ -651,13 +807,13 @@ cudaError_t launch_tc(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
   ++na;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_splits, p.batch * p.hkv, (p.n + p.rows_per_tile - 1) / p.rows_per_tile);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = TcCfg<D, TERMS>::SMEM;
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
   cfg.attrs = attrs;
   cfg.numAttrs = na;
   count_launch();
-  return cudaLaunchKernelEx(&cfg, attn_tc05_kernel<D, CAUSAL, TERMS>, *pool_map, *kblk_map,
+  return cudaLaunchKernelEx(&cfg, attn_tc05_kernel<D, CAUSAL, TERMS, FP8>, *pool_map, *kblk_map,
                             *vblk_map, p);
 }
 
@@ -749,6 +905,12 @@ cudaError_t attention_tc_launch(const CUtensorMap* pool_map, const CUtensorMap* 
     return cudaErrorInvalidValue;
   }
   if (p.kv_terms == 2) return cudaErrorInvalidValue;
+  if (p.fp8) {
+    if (p.scales == nullptr) return cudaErrorInvalidValue;
+    if (p.d == 128) return launch_tc<128, false, 1, true>(pool_map, kblk_map, vblk_map, p, s, pdl);
+    if (p.d == 64) return launch_tc<64, false, 1, true>(pool_map, kblk_map, vblk_map, p, s, pdl);
+    return cudaErrorInvalidValue;
+  }
   if (p.d == 128) return launch_tc<128, false, 1>(pool_map, kblk_map, vblk_map, p, s, pdl);
   if (p.d == 64) return launch_tc<64, false, 1>(pool_map, kblk_map, vblk_map, p, s, pdl);
   return cudaErrorInvalidValue;

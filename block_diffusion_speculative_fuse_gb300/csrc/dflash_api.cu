@@ -65,6 +65,23 @@ int encode_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ERR_INVALID_ARG;
 }
 
+// 2-D uint8 map over [rows][cols] bytes (cols a multiple of 16), box
+// [box_rows][cols], no swizzle, zero fill out of bounds.
+int encode_map_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows) {
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || cols % 16 != 0 || cols > 256)
+    return DFLASH_ERR_INVALID_ARG;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(cols), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ERR_INVALID_ARG;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
@@ -301,7 +318,14 @@ size_t layer_pool_elems(const dflash_model_s* m, const dflash_kv* kv) {
 }
 
 void set_pool(const dflash_model_s* m, QkvEpi& e, const dflash_kv* kv, int layer) {
-  e.pool = static_cast<uint16_t*>(kv->pool) + layer_pool_elems(m, kv) * layer;
+  if (kv->dtype == 1) {
+    // E4M3 context cache: one byte per element, one scale per vector
+    e.pool = nullptr;
+    e.pool8 = static_cast<uint8_t*>(kv->pool) + layer_pool_elems(m, kv) * layer;
+    e.scales8 = kv->scales + layer_pool_elems(m, kv) / m->cfg.head_dim * layer;
+  } else {
+    e.pool = static_cast<uint16_t*>(kv->pool) + layer_pool_elems(m, kv) * layer;
+  }
   e.page_table = kv->page_table;
   e.max_pages = kv->max_pages;
   e.n_pages = kv->n_pages;
@@ -309,12 +333,49 @@ void set_pool(const dflash_model_s* m, QkvEpi& e, const dflash_kv* kv, int layer
   e.kv_terms = kv_terms_of(m->cfg);
 }
 
+// Attention kernel of a stack pass over `batch` requests of n block rows.
+// The drafter: all block rows per CTA, key splits from an occupancy model.
+// The target (causal): query tiles of 64/G block rows and fixed 512-key
+// splits, chosen per cache (never per call), so block verify and one-token
+// decode run the same per-row arithmetic.
+struct AttnPlan {
+  bool use_tc;       // tcgen05 kernel (else mma.sync)
+  int split_pages;   // pages per key split (tcgen05)
+  int rows_per_tile; // block rows per query tile (tcgen05)
+  int splits;        // key splits per (request, KV head) (tcgen05)
+  uint64_t pool_rows;
+};
+
+AttnPlan attn_plan(const dflash_model_s* m, const dflash_kv* kv, int batch, int n) {
+  const dflash_config& c = m->cfg;
+  const int terms = kv_terms_of(c);
+  const int G = c.n_q_heads / c.n_kv_heads;
+  AttnPlan a;
+  const int tc_pages = kv->max_pages + (m->is_draft ? (n + 15) / 16 : 0);
+  a.split_pages = m->is_draft ? attention_tc_split_pages(c.head_dim, batch * c.n_kv_heads, tc_pages)
+                              : attention_tc_target_split_pages();
+  const int tc_splits = (tc_pages + a.split_pages - 1) / a.split_pages;
+  a.splits = tc_splits;
+  a.rows_per_tile = m->is_draft ? n : std::max(1, 64 / G);
+  a.pool_rows = static_cast<uint64_t>(c.n_layers) * kv->n_pages * 2 * terms * c.n_kv_heads * 16;
+  a.use_tc = m->attn_tc && a.pool_rows + 16 < (1ull << 31) &&
+             (m->is_draft ? attention_tc_ok(c.head_dim, c.n_q_heads, c.n_kv_heads, n, c.page_size,
+                                            a.split_pages)
+                          : ((c.head_dim == 64 || c.head_dim == 128) && G <= 64 &&
+                             tc_splits <= kMaxAttnCluster));
+  return a;
+}
+
 int check_kv(const dflash_model_s* m, const dflash_kv* kv) {
   if (kv == nullptr || kv->pool == nullptr || kv->page_table == nullptr || kv->n_pages <= 0 ||
-      kv->max_pages <= 0 || kv->n_rows <= 0)
+      kv->max_pages <= 0 || kv->n_rows <= 0 || (kv->dtype != 0 && kv->dtype != 1))
     return DFLASH_ERR_INVALID_ARG;
   if (!aligned16(kv->pool)) return DFLASH_ERR_INVALID_ARG;
-  (void)m;
+  if (kv->dtype == 1) {
+    // E4M3 caches: drafter context caches with one-term K/V only
+    if (kv->scales == nullptr || !aligned16(kv->scales)) return DFLASH_ERR_INVALID_ARG;
+    if (!m->is_draft || kv_terms_of(m->cfg) != 1) return DFLASH_ERR_UNSUPPORTED;
+  }
   return DFLASH_OK;
 }
 
@@ -351,29 +412,20 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
   const int rows = batch * n;
   const int H = c.hidden;
   const int max_keys = kv->max_pages * c.page_size;
-  // attention on tcgen05: tensor maps over the pool and the block K/V.  The
-  // drafter: all block rows per CTA, key splits from an occupancy model.  The
-  // target (causal): query tiles of 64/G block rows and fixed 512-key splits,
-  // chosen per cache (never per call), so block verify and one-token decode
-  // run the same per-row arithmetic.
+  // attention on tcgen05: tensor maps over the pool and the block K/V
   const int terms = kv_terms_of(c);
-  const int G = c.n_q_heads / c.n_kv_heads;
-  const int tc_pages = kv->max_pages + (m->is_draft ? (n + 15) / 16 : 0);
-  const int tc_split_pages = m->is_draft
-                                 ? attention_tc_split_pages(c.head_dim, batch * c.n_kv_heads, tc_pages)
-                                 : attention_tc_target_split_pages();
-  const int tc_splits = (tc_pages + tc_split_pages - 1) / tc_split_pages;
-  const int tc_rows_per_tile = m->is_draft ? n : std::max(1, 64 / G);
-  const uint64_t pool_rows = static_cast<uint64_t>(c.n_layers) * kv->n_pages * 2 * terms *
-                             c.n_kv_heads * 16;
-  const bool use_tc = m->attn_tc && pool_rows + 16 < (1ull << 31) &&
-                      (m->is_draft ? attention_tc_ok(c.head_dim, c.n_q_heads, c.n_kv_heads, n,
-                                                     c.page_size, tc_split_pages)
-                                   : ((c.head_dim == 64 || c.head_dim == 128) && G <= 64 &&
-                                      tc_splits <= kMaxAttnCluster));
+  const AttnPlan plan = attn_plan(m, kv, batch, n);
+  const int tc_split_pages = plan.split_pages;
+  const int tc_rows_per_tile = plan.rows_per_tile;
+  const uint64_t pool_rows = plan.pool_rows;
+  const bool use_tc = plan.use_tc;
+  const int tc_splits = plan.splits;
+  const bool fp8 = kv->dtype == 1;
+  if (fp8 && !use_tc) return DFLASH_ERR_UNSUPPORTED;  // E4M3 caches: tcgen05 attention only
   CUtensorMap pool_map, kblk_map, vblk_map;
   if (use_tc) {
-    int rc = encode_map(&pool_map, kv->pool, pool_rows, c.head_dim, c.head_dim, 16);
+    int rc = fp8 ? encode_map_u8(&pool_map, kv->pool, pool_rows, c.head_dim, 16)
+                 : encode_map(&pool_map, kv->pool, pool_rows, c.head_dim, c.head_dim, 16);
     if (!rc)
       rc = encode_map(&kblk_map, b.kblk, static_cast<uint64_t>(rows) * c.n_kv_heads, c.head_dim,
                       c.head_dim, 16);
@@ -434,6 +486,8 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       a.rows_per_tile = tc_rows_per_tile;
       a.causal = m->is_draft ? 0 : 1;
       a.kv_terms = terms;
+      a.fp8 = fp8 ? 1 : 0;
+      a.scales = kv->scales;
       a.out = b.o;
       a.out_lo = b.o_lo;
       a.status = ws.status();
@@ -812,6 +866,9 @@ int dflash_draft_block(dflash_model m, const int32_t* anchor, const int32_t* anc
   int rc = check_kv(m, kv);
   if (rc) return rc;
   if (batch > kv->n_rows) return DFLASH_ERR_CAPACITY;
+  // E4M3 caches: tcgen05 attention only (refused before anything launches)
+  if (kv->dtype == 1 && !attn_plan(m, kv, batch, m->cfg.block).use_tc)
+    return DFLASH_ERR_UNSUPPORTED;
   const dflash_config& c = m->cfg;
   const int B = c.block;
   const int rows = batch * B;
@@ -868,6 +925,23 @@ int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t ba
   DF_CUDA(verify_launch(draft, target, batch, B, out_tokens, n_accept, tgt_len_in, tgt_len_out,
                         ctx_pending, anchor_out, anchor_pos_in, anchor_pos_out, ctx_pos,
                         static_cast<cudaStream_t>(stream), true));
+  return DFLASH_OK;
+}
+
+int dflash_kv_quantize(dflash_model m, const dflash_kv* src, const dflash_kv* dst, void* stream) {
+  if (m == nullptr || src == nullptr || dst == nullptr || src->pool == nullptr ||
+      dst->pool == nullptr || dst->scales == nullptr || src->dtype != 0 || dst->dtype != 1 ||
+      src->n_pages != dst->n_pages || src->n_pages <= 0)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(src->pool) || !aligned16(dst->pool) || !aligned16(dst->scales))
+    return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = m->cfg;
+  if (kv_terms_of(c) != 1) return DFLASH_ERR_UNSUPPORTED;
+  const size_t vectors = static_cast<size_t>(c.n_layers) * src->n_pages * 2 * c.n_kv_heads *
+                         c.page_size;
+  DF_CUDA(kv_quantize_launch(static_cast<const uint16_t*>(src->pool),
+                             static_cast<uint8_t*>(dst->pool), dst->scales, vectors, c.head_dim,
+                             static_cast<cudaStream_t>(stream), true));
   return DFLASH_OK;
 }
 

@@ -389,7 +389,39 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
         }
       }
     }
+    // E4M3 context cache: amax of the head vector's bf16 values over its 8
+    // lanes (every lane takes part in the shuffles)
+    float am = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < P) am = fmaxf(am, fmaxf(fabsf(bf2f(f2bf(x1[j]))), fabsf(bf2f(f2bf(x2[j])))));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
     if (!act) continue;
+    if (kind > 0 && !is_blk && e.pool8 != nullptr) {
+      const float scale = am > 0.f ? am / 448.f : 1.f;
+      const size_t vecid = (static_cast<size_t>(pg) * 2 + (kind - 1)) * hkv * e.page_size +
+                           static_cast<size_t>(hidx) * e.page_size + pos % e.page_size;
+      uint8_t* d8 = e.pool8 + vecid * d + c0;
+      uint16_t c1[4], c2[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        c1[j] = e4m3x2_encode(bf2f(f2bf(x1[2 * j])) / scale, bf2f(f2bf(x1[2 * j + 1])) / scale);
+        c2[j] = e4m3x2_encode(bf2f(f2bf(x2[2 * j])) / scale, bf2f(f2bf(x2[2 * j + 1])) / scale);
+      }
+      if (P == 8) {
+        *reinterpret_cast<uint2*>(d8) = make_uint2(c1[0] | (static_cast<uint32_t>(c1[1]) << 16),
+                                                   c1[2] | (static_cast<uint32_t>(c1[3]) << 16));
+        *reinterpret_cast<uint2*>(d8 + half) = make_uint2(c2[0] | (static_cast<uint32_t>(c2[1]) << 16),
+                                                          c2[2] | (static_cast<uint32_t>(c2[3]) << 16));
+      } else {
+        *reinterpret_cast<uint32_t*>(d8) = c1[0] | (static_cast<uint32_t>(c1[1]) << 16);
+        *reinterpret_cast<uint32_t*>(d8 + half) = c2[0] | (static_cast<uint32_t>(c2[1]) << 16);
+      }
+      if (sub == 0) e.scales8[vecid] = scale;
+      continue;
+    }
     uint16_t* dst;
     uint16_t* dst_lo = nullptr;  // low terms (two-term cache)
     if (kind == 0) {

@@ -53,6 +53,8 @@ struct QkvEpi {
   int max_pages, n_pages, page_size;
   int n_req;             // rows of page_table: explicit pool_req values must lie in [0, n_req)
   int kv_terms;          // 1: bf16 K/V planes; 2: also bf16 low terms (planes 2, 3)
+  uint8_t* pool8;        // E4M3 context cache (layer base) instead of pool, or null
+  float* scales8;        // its per-vector scales (layer base)
   float2 rope[kMaxRopePairs];  // inv_freq of pair p as (hi, lo) float pair
 };
 
@@ -147,10 +149,11 @@ struct AttnParams {
 };
 cudaError_t attention_launch(const AttnParams& p, cudaStream_t s, bool pdl);
 
-// Non-causal drafter attention on tcgen05 (attention_tc05.cu).  K/V come from
-// three 2-D bf16 tensor maps (box 16 rows x 64 columns, 128-byte swizzle):
-// the whole pool viewed as [n_layers*n_pages*2*hkv*16][d] rows, and the
-// block keys/values viewed as [batch*hkv*n][d].
+// Attention on tcgen05 (attention_tc05.cu).  K/V come from three 2-D tensor
+// maps: the whole pool viewed as [n_layers*n_pages*planes*hkv*16][d] rows
+// (bf16: box 16 rows x 64 columns, 128-byte swizzle; E4M3 codes: uint8, box
+// 16 rows x d bytes, no swizzle), and the block keys/values viewed as bf16
+// [batch*hkv*n][d].
 struct AttnTcParams {
   const uint16_t* q;     // [batch*n][hq][d]
   int batch, n;          // requests, block rows per request
@@ -165,6 +168,8 @@ struct AttnTcParams {
   int rows_per_tile;     // block rows per CTA (grid.z = query tiles); the drafter: n
   int causal;            // 1: target pass (pool keys [0, pos0 + i] for row i; no block keys)
   int kv_terms;          // 2: the pool pages hold K, V, K_lo, V_lo planes (causal only)
+  int fp8;               // 1: pool_map is a uint8 map of E4M3 codes (box 16 rows x d bytes)
+  const float* scales;   // E4M3: per-vector scales, indexed like the pool map's rows
   uint16_t* out;         // [batch*n][hq][d]
   uint16_t* out_lo;      // optional low halves
   int32_t* status;
@@ -209,6 +214,9 @@ cudaError_t synth_target_launch(const int32_t* draft, int batch, int B, const ui
                                 int vocab, uint64_t seed, int64_t* step, int advance,
                                 int32_t* target, cudaStream_t s, bool pdl);
 cudaError_t copy_rows_f32_launch(const float* src, float* dst, size_t n, cudaStream_t s, bool pdl);
+// bf16 pool -> E4M3 codes + per-vector scales (vectors of d values)
+cudaError_t kv_quantize_launch(const uint16_t* src, uint8_t* dst, float* scales, size_t vectors,
+                               int d, cudaStream_t s, bool pdl);
 // sampling.cu: verify at temperature T > 0 (stats: batch*(2B-1) double2), and
 // categorical draws from softmax(logits / T) of the used rows of a blocked
 // logits array (stats: n_used double2)

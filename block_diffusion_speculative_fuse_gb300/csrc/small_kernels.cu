@@ -283,6 +283,35 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+// ---- E4M3 context cache: one warp per cached vector (position, K|V, head)
+// of d bf16 values: scale = amax / 448 (1 for a zero vector), codes of
+// value / scale rounded to nearest, ties to even, saturating.
+__global__ void __launch_bounds__(256)
+    kv_quantize_kernel(const uint16_t* src, uint8_t* dst, float* scales, size_t vectors, int d) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const size_t vec = static_cast<size_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (vec >= vectors) return;
+  const int per = d / 32;  // 2 or 4 values per lane
+  const uint16_t* s = src + vec * d + lane * per;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < per; ++j) v[j] = bf2f(s[j]);
+  float a = 0.f;
+  for (int j = 0; j < per; ++j) a = fmaxf(a, fabsf(v[j]));
+  a = warp_max(a);
+  const float scale = a > 0.f ? a / 448.f : 1.f;
+  uint8_t* o = dst + vec * d + lane * per;
+  if (per == 4) {
+    const uint32_t c = static_cast<uint32_t>(e4m3x2_encode(v[0] / scale, v[1] / scale)) |
+                       (static_cast<uint32_t>(e4m3x2_encode(v[2] / scale, v[3] / scale)) << 16);
+    *reinterpret_cast<uint32_t*>(o) = c;
+  } else {
+    *reinterpret_cast<uint16_t*>(o) = e4m3x2_encode(v[0] / scale, v[1] / scale);
+  }
+  if (lane == 0) scales[vec] = scale;
+}
+
 // ---- synthetic target (counter-based, splitmix64 output function)
 __device__ __forceinline__ uint64_t splitmix64(uint64_t z) {
   z += 0x9E3779B97F4A7C15ull;
@@ -365,6 +394,13 @@ cudaError_t argmax_reduce_launch(const float* val, const int32_t* idx, int rows,
                                  bool pdl) {
   return launch(argmax_reduce_kernel, dim3((rows + 3) / 4), dim3(128), 0, s, pdl, val, idx, rows,
                 n_tiles, block, out, skip_first);
+}
+cudaError_t kv_quantize_launch(const uint16_t* src, uint8_t* dst, float* scales, size_t vectors,
+                               int d, cudaStream_t s, bool pdl) {
+  const size_t blocks = (vectors + 7) / 8;
+  if (blocks == 0 || blocks > 0x7FFFFFFFu) return cudaErrorInvalidValue;
+  return launch(kv_quantize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, pdl, src,
+                dst, scales, vectors, d);
 }
 cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int batch, int B,
                           int32_t* out_tokens, int32_t* n_accept, const int32_t* tgt_len_in,

@@ -68,23 +68,70 @@ class DeviceModel:
 
 
 class PagedKV:
-    """A paged KV pool [L][n_pages][2*kv_terms][hkv][page][d] (bf16) and page
-    table (planes K, V, then the low terms of K and V for a two-term cache)."""
+    """A paged KV pool [L][n_pages][2*kv_terms][hkv][page][d] and page table
+    (planes K, V, then the low terms of K and V for a two-term cache).
+
+    dtype "bf16": the pool holds bf16 values.  dtype "e4m3" (drafter context
+    caches): the pool holds uint8 E4M3 codes [L][n_pages][2][hkv][page][d]
+    and `scales` fp32 [L][n_pages][2][hkv][page], one per cached vector."""
 
     def __init__(self, shape, page_table: np.ndarray, n_pages: int, page_size=16,
-                 device="cuda", zero=True):
+                 device="cuda", zero=True, dtype="bf16"):
         L, hkv, d = shape.n_layers, shape.n_kv_heads, shape.head_dim
         planes = 2 * getattr(shape, "kv_terms", 1)
         alloc = torch.zeros if zero else torch.empty
-        self.pool = alloc((L, n_pages, planes, hkv, page_size, d), dtype=torch.bfloat16,
-                          device=device)
+        if dtype not in ("bf16", "e4m3"):
+            raise ValueError(f"unknown cache dtype {dtype!r}")
+        if dtype == "e4m3" and planes != 2:
+            raise ValueError("E4M3 caches hold one term of K and V")
+        self.dtype = dtype
+        self.scales = None
+        if dtype == "bf16":
+            self.pool = alloc((L, n_pages, planes, hkv, page_size, d), dtype=torch.bfloat16,
+                              device=device)
+        else:
+            self.pool = alloc((L, n_pages, 2, hkv, page_size, d), dtype=torch.uint8, device=device)
+            self.scales = alloc((L, n_pages, 2, hkv, page_size), dtype=torch.float32,
+                                device=device)
         self.table_np = np.ascontiguousarray(page_table, dtype=np.int32)
         self.table = torch.from_numpy(self.table_np).to(device)
         self.page_size = page_size
         self.n_pages = n_pages
         self.struct = B.DflashKV(pool=self.pool.data_ptr(), page_table=self.table.data_ptr(),
                                  n_pages=n_pages, max_pages=self.table_np.shape[1],
-                                 n_rows=self.table_np.shape[0])
+                                 n_rows=self.table_np.shape[0],
+                                 dtype=0 if dtype == "bf16" else 1,
+                                 scales=self.scales.data_ptr() if self.scales is not None else None)
+
+    def quantized(self, model):
+        """A new E4M3 cache with this bf16 cache's pages and table, every
+        vector converted on the device (dflash_kv_quantize)."""
+        if self.dtype != "bf16":
+            raise ValueError("only a bf16 cache converts to E4M3")
+        L, n_pages, _, hkv, page, d = self.pool.shape
+        q = PagedKV.__new__(PagedKV)
+        q.dtype = "e4m3"
+        q.pool = torch.empty((L, n_pages, 2, hkv, page, d), dtype=torch.uint8,
+                             device=self.pool.device)
+        q.scales = torch.empty((L, n_pages, 2, hkv, page), dtype=torch.float32,
+                               device=self.pool.device)
+        q.table_np, q.table = self.table_np, self.table
+        q.page_size, q.n_pages = self.page_size, self.n_pages
+        q.struct = B.DflashKV(pool=q.pool.data_ptr(), page_table=q.table.data_ptr(),
+                              n_pages=self.n_pages, max_pages=self.struct.max_pages,
+                              n_rows=self.struct.n_rows, dtype=1, scales=q.scales.data_ptr())
+        B.dflash_kv_quantize(model.handle, self.struct, q.struct)
+        return q
+
+    def read_codes(self, layer: int, req: int, n: int):
+        """E4M3 cache: codes [n][2][hkv][d] (uint8) and scales [n][2][hkv] of
+        one request's logical positions 0..n-1, on the host."""
+        P = self.page_size
+        idx = torch.arange(n, device=self.pool.device)
+        pages = self.table[req].long()[idx // P]
+        codes = self.pool[layer, pages, :, :, idx % P]
+        scales = self.scales[layer, pages, :, :, idx % P]
+        return codes.cpu().numpy(), scales.cpu().numpy()
 
     def fill_logical(self, layer: int, req: int, k_u16: np.ndarray, v_u16: np.ndarray):
         """Place already-projected context K/V ([len][hkv][d], bf16 bits) of

@@ -19,7 +19,7 @@ from .device import DeviceModel, PagedKV, i32, to_device_u16
 
 class DraftStep:
     def __init__(self, wl, device="cuda", keep_host=False, model=None, weights=None,
-                 shared=None):
+                 shared=None, kv_dtype="bf16"):
         self.wl = wl
         d = wl.draft
         self.shape = d
@@ -53,6 +53,11 @@ class DraftStep:
                 if keep_host:
                     ctx_k[(l, r)] = k
                     ctx_v[(l, r)] = v
+        if kv_dtype == "e4m3":
+            # the synthetic context is laid out in bf16, then converted on the device
+            self.kv = self.kv.quantized(model)
+        elif kv_dtype != "bf16":
+            raise ValueError(f"unknown cache dtype {kv_dtype!r}")
         taps = W.taps_bf16(self.T, d, wid)
         req = np.repeat(np.arange(b, dtype=np.int32), self.new_rows)
         pos = np.concatenate([np.arange(c, c + t, dtype=np.int32)

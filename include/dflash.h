@@ -137,6 +137,16 @@ typedef struct {
   int32_t n_pages;
   int32_t max_pages;
   int32_t n_rows;
+  /* 0: the pool holds bf16 K/V.  1 (drafter context caches): the pool holds
+   * E4M3 codes, uint8 [n_layers][n_pages][2][n_kv_heads][page_size][head_dim],
+   * and `scales` fp32 [n_layers][n_pages][2][n_kv_heads][page_size] one scale
+   * per (position, head) of K and of V: value = decode(code) * scale, with
+   * scale = amax / 448 of the vector's bf16 values (1 for a zero vector) and
+   * codes rounded to nearest, ties to even, saturating at +-448 ("DFlash-2:
+   * z-lab boosts speculative decoding throughput...", section on the
+   * precision cost: an 8-bit KV cache against a 16-bit one). */
+  int32_t dtype;
+  float* scales;
 } dflash_kv;
 
 /* ------------------------------------------------------------------ model */
@@ -214,7 +224,13 @@ int dflash_ctx_fuse_noalloc(dflash_model m, const void* taps, int32_t T, void* c
  * Outputs: draft int32 [batch][B-1] (argmax of rows 1..B-1, lowest index on
  * ties); optional logits fp32 [batch*B][vocab] and hidden fp32
  * [batch*B][hidden] (final residual stream before the final norm) for
- * checking; pass NULL to skip them. */
+ * checking; pass NULL to skip them.
+ * With an E4M3 cache (kv->dtype 1) the pending rows are stored as codes and
+ * scales, and attention decodes the context keys exactly (code * scale; the
+ * block's own K/V stay bf16).  Only the tcgen05 attention reads E4M3 caches:
+ * a shape or model it does not take (more than 128 query rows per KV head,
+ * head_dim other than 64/128, the mma.sync kernel selected at model
+ * creation) gives DFLASH_ERR_UNSUPPORTED before any launch. */
 int dflash_draft_block(dflash_model m, const int32_t* anchor, const int32_t* anchor_pos,
                        int32_t batch, const dflash_kv* kv, const void* pending_ctx,
                        const int32_t* pending_req, const int32_t* pending_pos, int32_t T,
@@ -246,6 +262,16 @@ int dflash_verify_greedy(const int32_t* draft, const int32_t* target, int32_t ba
                          int32_t* tgt_len_out, int32_t* ctx_pending, int32_t* anchor_out,
                          const int32_t* anchor_pos_in, int32_t* anchor_pos_out, int32_t* ctx_pos,
                          void* stream);
+
+/* Converts a bf16 cache (src, dtype 0) into an E4M3 cache (dst, dtype 1,
+ * with scales) of the same geometry, for the model m: every position of every
+ * page and layer (the layout and rounding are those of dflash_kv).  Pages and
+ * page table are taken as they are; nothing but dst's pool and scales is
+ * written.  DFLASH_ERR_INVALID_ARG (nothing launched): a null pointer, a pool
+ * or scale array not 16-byte aligned, src not bf16, dst not E4M3, or page
+ * counts that differ; DFLASH_ERR_UNSUPPORTED for a two-term cache.  src and
+ * dst must not overlap. */
+int dflash_kv_quantize(dflash_model m, const dflash_kv* src, const dflash_kv* dst, void* stream);
 
 /* Verification at temperature T > 0 ("DFlash: how block diffusion boosts
  * NVIDIA Blackwell throughput", section "Real-world integration": sampling-
