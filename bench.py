@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--accept-sample", type=int, default=200)
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"],
+                    help="drafter context cache: bf16, or E4M3 codes with per-vector scales")
     return ap.parse_args()
 
 
@@ -57,20 +59,21 @@ def peaks():
 
 
 # ------------------------------------------------------------ accounting
-def step_bytes(wl, ctx_before, new_rows):
+def step_bytes(wl, ctx_before, new_rows, kv="bf16"):
     """Algorithmic HBM bytes of one step: every weight once, the context K/V
     read once per layer, the appended K/V written once, the step's inputs and
-    outputs."""
+    outputs.  An E4M3 cache holds one byte per element and a 4-byte scale
+    per (position, head) vector."""
     d = wl.draft
     H, kvd = d.hidden, d.kv_dim
     weights = (H * d.n_taps * H + H) + d.n_layers * d.layer_params() + H + H \
         + d.vocab * H + d.n_layers * H * d.conv_width
     L_after = np.asarray(ctx_before) + np.asarray(new_rows)
-    kv_read = int(L_after.sum()) * 2 * kvd * d.n_layers
-    kv_write = int(np.sum(new_rows)) * 2 * kvd * d.n_layers
+    kv_elems = (int(L_after.sum()) + int(np.sum(new_rows))) * 2 * kvd * d.n_layers
+    kv_b = 2.0 if kv == "bf16" else 1.0 + 4.0 / d.head_dim
     taps = int(np.sum(new_rows)) * d.n_taps * H
     emb = wl.batch * H
-    return 2 * (weights + kv_read + kv_write + taps + emb)
+    return int(2 * (weights + taps + emb) + kv_b * kv_elems)
 
 
 def step_flops(wl, ctx_before, new_rows):
@@ -278,6 +281,33 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------ our arm
+def e4m3_vs_bf16(st, wl, stream):
+    """The draft of one step with the E4M3 context cache against the same
+    step (same weights, inputs and context) over a bf16 cache: the fraction
+    of drafted tokens that agree, and the mean length of the matching prefix
+    of each request's block, which is the number of drafts an E4M3 drafter
+    gets accepted by a target that accepts exactly the bf16 drafter's block.
+    With random-init weights the logits are nearly flat, so this understates
+    the agreement of a trained drafter."""
+    import torch
+
+    from block_diffusion_speculative_fuse_gb300.session import DraftStep
+    st16 = DraftStep(wl, model=st.model)
+    with torch.cuda.stream(stream):
+        st.fuse(stream)
+        st.draft_block(stream=stream, append=True)
+        st16.fuse(stream)
+        st16.draft_block(stream=stream, append=True)
+    stream.synchronize()
+    a, b = st.draft.cpu().numpy(), st16.draft.cpu().numpy()
+    same = a == b
+    prefix = np.where(same.all(1), same.shape[1], np.argmin(same, axis=1))
+    del st16
+    return {"drafted_token_agreement": float(same.mean()),
+            "mean_matching_prefix": float(prefix.mean()), "block_drafts": int(same.shape[1]),
+            "requests": int(same.shape[0])}
+
+
 def run_ours(args, rank, world, dist):
     import torch
 
@@ -290,7 +320,7 @@ def run_ours(args, rank, world, dist):
     B.load()
     wl = W.get_workload(args.config)
     d = wl.draft
-    st = DraftStep(wl)
+    st = DraftStep(wl, kv_dtype=args.kv)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -402,11 +432,15 @@ def run_ours(args, rank, world, dist):
     e5.synchronize()
     ms_lm = e4.elapsed_time(e5) / nl
 
+    kv_cmp = None
+    if args.kv == "e4m3":
+        kv_cmp = e4m3_vs_bf16(st, wl, stream)
+
     if rank != 0:
         return
     pk, pk_kind = peaks()
     hbm = float(pk["hbm_gbs"])
-    sb = step_bytes(wl, st.ctx_before, st.new_rows)
+    sb = step_bytes(wl, st.ctx_before, st.new_rows, args.kv)
     sf = step_flops(wl, st.ctx_before, st.new_rows)
     steps_per_s = 1e3 / ms
     drafted = steps_per_s * wl.batch * (d.block - 1) * world
@@ -423,7 +457,7 @@ def run_ours(args, rank, world, dist):
         "config": {"workload": wl.name, "batch": wl.batch, "block": d.block,
                    "ctx_len": int(st.ctx_before.max()), "new_ctx_rows": int(st.T),
                    "draft_layers": d.n_layers, "hidden": d.hidden, "vocab": d.vocab,
-                   "cuda_graph": graph is not None,
+                   "kv_cache": args.kv, "cuda_graph": graph is not None,
                    "l2": "inputs larger than L2: %.2f GB streamed per step" % (sb / 1e9)},
         "steps_per_s": steps_per_s,
         "drafted_tokens_per_s": drafted,
@@ -444,6 +478,8 @@ def run_ours(args, rank, world, dist):
         "launches_per_step": int(launches_per_step),
         "clocks": clocks,
     }
+    if kv_cmp is not None:
+        line["kv_e4m3_vs_bf16"] = kv_cmp
     if world == 1 and not args.no_cpu_baseline:
         host = host_inputs_for_oracle(wl)
         sec = time_oracle(wl, host, 1, 0)
@@ -551,6 +587,8 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
     elif W.get_workload(args.config).target is not None:
+        if args.kv != "bf16":
+            raise SystemExit("--kv e4m3 applies to the draft-step workloads only")
         run_e2e(args, rank, world)
     else:
         run_ours(args, rank, world, dist)

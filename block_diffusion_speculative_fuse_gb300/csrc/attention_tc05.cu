@@ -50,13 +50,14 @@ constexpr int kThreads = 192;      // warps 0-3 softmax, 4 TMA, 5 MMA
 // TERMS = 2: every key chunk also carries the low bf16 terms of K and V
 // (planes K, V, K_lo, V_lo in a stage, as in the pool's pages).
 // FP8: the context pages hold E4M3 codes and per-vector scales; they arrive
-// in a ring of code stages and two converter warps turn them into the bf16
+// in a ring of code stages and eight converter warps turn them into the bf16
 // stages the MMAs read (block keys arrive there as bf16 directly).
 template <int D, int TERMS = 1, bool FP8 = false>
 struct TcCfg {
-  static constexpr int THREADS = FP8 ? 256 : 192;  // + warps 6-7: converters
-  static constexpr int STAGES = (TERMS == 2 || FP8) ? 2 : 4;
-  static constexpr int F8_STAGES = FP8 ? 4 : 0;
+  static constexpr int CONV_THREADS = 256;        // FP8: warps 6-13 convert
+  static constexpr int THREADS = FP8 ? 192 + CONV_THREADS : 192;
+  static constexpr int STAGES = TERMS == 2 ? 2 : (FP8 ? 3 : 4);
+  static constexpr int F8_STAGES = FP8 ? 3 : 0;
   static constexpr int K8_BYTES = kChunkKeys * D;               // [64 keys][D] codes
   static constexpr int F8_STAGE_BYTES = 2 * K8_BYTES;           // K codes then V codes
   static constexpr int SC_BYTES = 2 * kChunkKeys * 4;           // K scales then V scales
@@ -88,6 +89,10 @@ struct TcCfg {
   static constexpr uint32_t S_COL0 = 0, O_COL = 128;
 };
 
+// v[i] for a run-time i in [0, 4) without indexing a local array
+__device__ __forceinline__ int pick4(const int (&v)[4], int i) {
+  return i == 0 ? v[0] : i == 1 ? v[1] : i == 2 ? v[2] : v[3];
+}
 __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
   return static_cast<uint32_t>(row * 128 + ((chunk16 ^ (row & 7)) << 4));
 }
@@ -145,14 +150,14 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // FP8: a bf16 stage is complete when both converter warps have arrived
+      // FP8: a bf16 stage is complete when every converter warp has arrived
       // (and the bf16 block keys they requested have landed)
-      mbar_init(&kv_full[s], FP8 ? 2 : 1);
+      mbar_init(&kv_full[s], FP8 ? C::CONV_THREADS / 32 : 1);
       mbar_init(&kv_empty[s], 1);
     }
     for (int s = 0; s < C::F8_STAGES; ++s) {
       mbar_init(&f8_full[s], 1);
-      mbar_init(&f8_empty[s], 2);
+      mbar_init(&f8_empty[s], C::CONV_THREADS / 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -294,12 +299,25 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
       for (int c = max(0, issued - S8); c < issued; ++c)
         mbar_wait(&f8_full[c % S8], (c / S8) & 1, nullptr);
   } else if (FP8 && warp >= 6) {
-    // ------------------------------------------------ converters: code stage ->
-    // bf16 stage (exact values; invalid keys as zeros), per-key scales, and
-    // the bf16 block keys by TMA (first lane)
+    // ------------------------------------------------ converters (warps 6..): code
+    // stage -> bf16 stage (exact values; invalid keys as zeros), per-key
+    // scales, and the bf16 block keys by TMA (first thread).  Thread t owns
+    // the 8-code piece c8 = t % CH of key rows r0 + RPP*i (i = 0, 1, ...) of
+    // K and of V, so a piece's page, its row within the page and its
+    // 128-byte swizzle phase are fixed per thread; the page ids and valid
+    // counts of the chunk are read once into registers.
     constexpr int S8 = C::F8_STAGES > 0 ? C::F8_STAGES : 1;
+    constexpr int NT = C::CONV_THREADS;
+    constexpr int CH = D / 8;                     // 8-code pieces per key row
+    constexpr int RPP = NT / CH;                  // key rows per pass
+    constexpr int JPK = kChunkKeys / RPP;         // passes per plane (K or V)
+    static_assert(RPP % 8 == 0 && NT >= 2 * kChunkKeys, "converter thread mapping");
     const uint64_t pol = l2_policy_evict_first();
     const int t = tid - 192;
+    const int c8 = t % CH, r0 = t / CH;
+    const uint32_t f8_base = smem_u32(sm + C::F8_OFF) + r0 * D + c8 * 8;
+    const uint32_t b16_base = smem_u32(sm + C::KV_OFF) + r0 * 128 + (c8 / 8) * C::KV_HALF +
+                              (((c8 % 8) ^ (r0 % 8)) << 4);
     int done_c = 0;
     for (int c = 0; c < nch; ++c) {
       const int st8 = c % S8, sb = c % kStages;
@@ -311,16 +329,18 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
         if (lane == 0) raise_status(p.status, DFLASH_ERR_TIMEOUT, 316);
         break;
       }
+      const int4 ids4 = *reinterpret_cast<const int4*>(pages_s + c * kChunkPages);
+      const int4 cnt4 = *reinterpret_cast<const int4*>(pages_n + c * kChunkPages);
+      const int idv[4] = {ids4.x, ids4.y, ids4.z, ids4.w};
+      const int cnv[4] = {cnt4.x, cnt4.y, cnt4.z, cnt4.w};
       if (t == 0) {
-        int nb = 0;
-#pragma unroll
-        for (int pp = 0; pp < kChunkPages; ++pp) nb += pages_s[c * kChunkPages + pp] <= -2 ? 1 : 0;
+        const int nb = (idv[0] <= -2) + (idv[1] <= -2) + (idv[2] <= -2) + (idv[3] <= -2);
         if (nb > 0) {
           mbar_expect_tx(&kv_full[sb], nb * 2 * C::HALVES * (16 * 64 * 2));
+#pragma unroll
           for (int pp = 0; pp < kChunkPages; ++pp) {
-            const int id = pages_s[c * kChunkPages + pp];
-            if (id > -2) continue;
-            const int y = (req * p.hkv + g) * p.n + (-2 - id) * 16;
+            if (idv[pp] > -2) continue;
+            const int y = (req * p.hkv + g) * p.n + (-2 - idv[pp]) * 16;
             for (int kv = 0; kv < 2; ++kv)
               for (int hf = 0; hf < C::HALVES; ++hf)
                 tma_load_2d(sm + C::KV_OFF + sb * C::STAGE_BYTES + kv * C::K_BYTES + hf * C::KV_HALF +
@@ -329,36 +349,46 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
           }
         }
       }
-      const uint8_t* f8 = sm + C::F8_OFF + st8 * C::F8_STAGE_BYTES;
-      uint8_t* b16 = sm + C::KV_OFF + sb * C::STAGE_BYTES;
-      constexpr int CH = D / 8;  // 8-value pieces per key row
-      for (int idx = t; idx < kChunkPages * 2 * 16 * CH; idx += 64) {
-        const int c16 = idx % CH, rest = idx / CH;
-        const int key = rest % 16, kv = (rest / 16) % 2, pp = rest / 32;
-        const int id = pages_s[c * kChunkPages + pp];
-        if (id <= -2) continue;  // block keys arrive as bf16
-        uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (id >= 0 && key < pages_n[c * kChunkPages + pp]) {
-          const uint2 cd = *reinterpret_cast<const uint2*>(f8 + kv * C::K8_BYTES + (pp * 16 + key) * D + c16 * 8);
-          o.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(cd.x & 0xFFFFu));
-          o.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(cd.x >> 16));
-          o.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(cd.y & 0xFFFFu));
-          o.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(cd.y >> 16));
+      const uint32_t src = f8_base + st8 * C::F8_STAGE_BYTES;
+      const uint32_t dst = b16_base + sb * C::STAGE_BYTES;
+#pragma unroll
+      for (int j0 = 0; j0 < 2 * JPK; j0 += 8) {
+        uint2 cd[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + u, kv = j / JPK, i = j % JPK;
+          if (j >= 2 * JPK) break;
+          cd[u] = ld_shared_u2(src + kv * C::K8_BYTES + RPP * i * D);
         }
-        *reinterpret_cast<uint4*>(b16 + kv * C::K_BYTES + (c16 / 8) * C::KV_HALF +
-                                  swz128(pp * 16 + key, c16 % 8)) = o;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + u, kv = j / JPK, i = j % JPK;
+          if (j >= 2 * JPK) break;
+          const int key = r0 + RPP * i, pp = key / 16;
+          // RPP <= 16: the page is fixed by i; else r0 picks one of two pages
+          const int id = RPP <= 16 ? idv[(RPP * i) / 16] : pick4(idv, pp);
+          const int cnt = RPP <= 16 ? cnv[(RPP * i) / 16] : pick4(cnv, pp);
+          if (id <= -2) continue;                      // block keys arrive as bf16
+          uint4 o = make_uint4(0u, 0u, 0u, 0u);
+          if (id >= 0 && key % 16 < cnt) {
+            o = make_uint4(e4m3x2_to_bf16x2(cd[u].x), e4m3x2_to_bf16x2(cd[u].x >> 16),
+                           e4m3x2_to_bf16x2(cd[u].y), e4m3x2_to_bf16x2(cd[u].y >> 16));
+          }
+          st_shared_u4(dst + kv * C::K_BYTES + RPP * i * 128, o);
+        }
       }
-      float* scb = reinterpret_cast<float*>(sm + C::SCB_OFF + sb * C::SC_BYTES);
-      const float* sc8 = reinterpret_cast<const float*>(sm + C::SC8_OFF + st8 * C::SC_BYTES);
-      for (int k = t; k < 2 * kChunkKeys; k += 64) {
-        const int key = k % kChunkKeys, pp = key / 16;
-        const int id = pages_s[c * kChunkPages + pp];
+      if (t < 2 * kChunkKeys) {
+        // per-key scales of the stage (K then V): 0 past a page's valid keys,
+        // 1 for block keys
+        const int key = t % kChunkKeys, pp = key / 16;
+        const int id = pick4(idv, pp), cnt = pick4(cnv, pp);
+        const float* sc8 = reinterpret_cast<const float*>(sm + C::SC8_OFF + st8 * C::SC_BYTES);
         float v = 0.f;
         if (id <= -2)
           v = 1.f;
-        else if (id >= 0 && (key % 16) < pages_n[c * kChunkPages + pp])
-          v = sc8[k];
-        scb[k] = v;
+        else if (id >= 0 && key % 16 < cnt)
+          v = sc8[t];
+        reinterpret_cast<float*>(sm + C::SCB_OFF + sb * C::SC_BYTES)[t] = v;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -517,13 +547,19 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
         s[j] = __uint_as_float(sr0[j]);
         s[32 + j] = __uint_as_float(sr1[j]);
       }
-      const float* sv = nullptr;  // FP8: the V scale of every key, folded into P
+      uint32_t sv_addr = 0;  // FP8: the V scale of every key, folded into P
       if constexpr (FP8) {
         // K scales folded into the scores (S = scale_k * (q . codes))
-        const float* sk = reinterpret_cast<const float*>(sm + C::SCB_OFF + st * C::SC_BYTES);
-        sv = sk + kChunkKeys;
+        const uint32_t sk_addr = smem_u32(sm + C::SCB_OFF + st * C::SC_BYTES);
+        sv_addr = sk_addr + kChunkKeys * 4;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) s[j] *= sk[j];
+        for (int j = 0; j < 64; j += 4) {
+          const float4 k4 = ld_shared_f4(sk_addr + j * 4);
+          s[j] *= k4.x;
+          s[j + 1] *= k4.y;
+          s[j + 2] *= k4.z;
+          s[j + 3] *= k4.w;
+        }
       }
       if (!full) {
         // invalid keys (stale or zero-filled rows) never contribute
@@ -578,12 +614,23 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
       const float neg = (m_used == -INFINITY) ? 0.f : -m_used;
       uint32_t pk[32];
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+      float svv[FP8 ? 64 : 1];
+      if constexpr (FP8) {
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+          const float4 v4 = ld_shared_f4(sv_addr + j * 4);
+          svv[j] = v4.x;
+          svv[j + 1] = v4.y;
+          svv[j + 2] = v4.z;
+          svv[j + 3] = v4.w;
+        }
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float p0 = ex2_approx(fmaf(s[2 * j], sl2, neg));
         const float p1 = ex2_approx(fmaf(s[2 * j + 1], sl2, neg));
         if constexpr (FP8)
-          pk[j] = pack_bf16x2(p0 * sv[2 * j], p1 * sv[2 * j + 1]);  // P * scale_v
+          pk[j] = pack_bf16x2(p0 * svv[2 * j], p1 * svv[2 * j + 1]);  // P * scale_v
         else
           pk[j] = pack_bf16x2(p0, p1);
         ls4[j & 3] += p0 + p1;

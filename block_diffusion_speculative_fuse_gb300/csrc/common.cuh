@@ -59,16 +59,34 @@ __device__ __forceinline__ uint16_t e4m3x2_encode(float lo, float hi) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// Two E4M3 codes (bits 0-7, 8-15) as two bf16 values packed the same way;
-// exact (E4M3 -> f16 -> f32 -> bf16, every E4M3 value has at most 4
-// significant bits and lies in the range of each format).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t codes) {
+// Two E4M3 codes (bits 0-7, 8-15) as two bf16 values packed the same way.
+// Exact: every E4M3 value has at most 4 significant bits and lies inside the
+// normal range of f16, f32 and bf16 (the hardware conversion to f16x2, then
+// f16 -> f32 -> bf16).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes) {
   uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(codes));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<unsigned short>(codes & 0xFFFFu)));
   const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
   const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
   __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&b);
+}
+__device__ __forceinline__ uint2 ld_shared_u2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
