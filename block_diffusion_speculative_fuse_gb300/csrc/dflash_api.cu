@@ -93,6 +93,7 @@ struct dflash_model_s {
   int sms = 148;
   bool is_draft = false;
   bool attn_tc = true;      // drafter attention on tcgen05 (attention_tc05.cu) when the shape allows
+  int two_term_layers = -1;  // layers [0, k) carry two-term (hi + lo) activations; -1: automatic
   // GEMM: k-blocks its producer still has to request when the next kernel
   // may launch (< 0: at the start)
   int dep_lead = 2;
@@ -191,7 +192,7 @@ size_t partial_floats(const dflash_model_s* m, int rows_main, int rows_qkv) {
   size_t mx = 0;
   for (const GemmShape& g : shapes) {
     if (g.K <= 0 || g.N <= 0 || g.m_rows <= 0) continue;
-    const int bn = gemm_bn_for(g.m_rows);
+    const int bn = gemm_bn_for(g.m_rows, g.N, m->sms);
     const int mt = (g.m_rows + bn - 1) / bn;
     const int s = choose_splits(m, g.N / kTileN, mt, g.K / kTileK, bn);
     // splits up to the cluster size reduce through DSMEM and need no buffer
@@ -272,7 +273,7 @@ GemmParams gemm_base(const dflash_model_s* m, int M, int N, int K, int bn, Ws& w
 // x_lo (optional): low bf16 halves of the activation operand, same layout as x.
 int run_gemm(const dflash_model_s* m, const CUtensorMap* wmap, const void* x, int ld_x,
              GemmParams& p, float* partial, cudaStream_t s, const void* x_lo = nullptr) {
-  const int bn = gemm_bn_for(p.M);
+  const int bn = gemm_bn_for(p.M, p.N, m->sms);
   const int mt = (p.M + bn - 1) / bn;
   p.cluster = 0;
   if (p.splits > 1) {
@@ -434,11 +435,21 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
                       c.head_dim, 16);
     if (rc) return rc;
   }
+  // Two-term (hi + lo bf16) activations for O, gate/up and down.  The
+  // target: every layer, for any row count (its per-row arithmetic must not
+  // depend on the batch).  The drafter: every layer while the pass has at
+  // most 64 block rows (its GEMMs then stream weights and the second term
+  // is free), else the first two layers, which carry most of the rounding
+  // error that reaches the logits.
+  const int two_layers = m->two_term_layers >= 0 ? m->two_term_layers
+                         : (m->is_draft && rows > 64) ? std::min(2, c.n_layers)
+                                                      : c.n_layers;
   for (int l = 0; l < c.n_layers; ++l) {
+    const bool two = l < two_layers;  // hi + lo activations in this layer
     // QKV (+ context K/V rows in the same weight pass)
     {
       const int M = rows + ctx_rows;
-      GemmParams p = gemm_base(m, M, m->qkv_rows, H, gemm_bn_for(M), ws);
+      GemmParams p = gemm_base(m, M, m->qkv_rows, H, gemm_bn_for(M, m->qkv_rows, m->sms), ws);
       p.w_row0 = l * m->qkv_rows;
       p.mode = EPI_QKV;
       set_norm_in(m, p, b.ssq_a, rows);
@@ -489,7 +500,7 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       a.fp8 = fp8 ? 1 : 0;
       a.scales = kv->scales;
       a.out = b.o;
-      a.out_lo = b.o_lo;
+      a.out_lo = two ? b.o_lo : nullptr;
       a.status = ws.status();
       DF_CUDA(attention_tc_launch(&pool_map, &kblk_map, &vblk_map, a, s, true));
     } else {
@@ -517,41 +528,41 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       a.o_part = b.o_part;
       a.ml_part = b.ml_part;
       a.out = b.o;
-      a.out_lo = b.o_lo;
+      a.out_lo = two ? b.o_lo : nullptr;
       a.status = ws.status();
       DF_CUDA(attention_launch(a, s, true));
     }
     // O projection + residual (+ DFlash-2 block conv) -> post-norm input
     {
-      GemmParams p = gemm_base(m, rows, H, m->q_dim, gemm_bn_for(rows), ws);
+      GemmParams p = gemm_base(m, rows, H, m->q_dim, gemm_bn_for(rows, H, m->sms), ws);
       p.w_row0 = l * H;
       set_resid_out(m, p, b.x, u16(m->w.post_norm) + static_cast<size_t>(l) * H, b.a2, b.ssq_a2);
-      p.xg_lo = b.a2_lo;
+      p.xg_lo = two ? b.a2_lo : nullptr;
       if (m->is_draft && c.conv_width > 0 && m->w.conv != nullptr) {
         p.conv = u16(m->w.conv) + static_cast<size_t>(l) * H * c.conv_width;
         p.conv_width = c.conv_width;
         p.block = n;
       }
-      int rc = run_gemm(m, &m->m_wo, b.o, m->q_dim, p, b.partial, s, b.o_lo);
+      int rc = run_gemm(m, &m->m_wo, b.o, m->q_dim, p, b.partial, s, two ? b.o_lo : nullptr);
       if (rc) return rc;
     }
     // gate/up + SwiGLU: each 128-row tile = 64 gate rows + the matching 64 up rows
     {
-      GemmParams p = gemm_base(m, rows, 2 * c.mlp, H, gemm_bn_for(rows), ws);
+      GemmParams p = gemm_base(m, rows, 2 * c.mlp, H, gemm_bn_for(rows, 2 * c.mlp, m->sms), ws);
       p.w_row0 = l * 2 * c.mlp;
       p.w_tile_step = 64;
       p.w_half_gap = c.mlp;
       p.mode = EPI_SWIGLU;
       p.out = b.hmid;
-      p.out_lo = b.hmid_lo;
+      p.out_lo = two ? b.hmid_lo : nullptr;
       p.ld_out = c.mlp;
       set_norm_in(m, p, b.ssq_a2, rows);
-      int rc = run_gemm(m, &m->m_gu, b.a2, H, p, b.partial, s, b.a2_lo);
+      int rc = run_gemm(m, &m->m_gu, b.a2, H, p, b.partial, s, two ? b.a2_lo : nullptr);
       if (rc) return rc;
     }
     // down projection + residual -> next layer's in-norm input (or final norm)
     {
-      GemmParams p = gemm_base(m, rows, H, c.mlp, gemm_bn_for(rows), ws);
+      GemmParams p = gemm_base(m, rows, H, c.mlp, gemm_bn_for(rows, H, m->sms), ws);
       p.w_row0 = l * H;
       const bool last = (l == c.n_layers - 1);
       const uint16_t* g = last ? u16(m->w.final_norm)
@@ -561,7 +572,7 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
         p.raw_out = taps + static_cast<size_t>(tap_slot[l]) * H;
         p.ld_raw = n_taps * H;
       }
-      int rc = run_gemm(m, &m->m_down, b.hmid, c.mlp, p, b.partial, s, b.hmid_lo);
+      int rc = run_gemm(m, &m->m_down, b.hmid, c.mlp, p, b.partial, s, two ? b.hmid_lo : nullptr);
       if (rc) return rc;
     }
   }
@@ -571,7 +582,7 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
 int run_lm_head(const dflash_model_s* m, Ws& ws, StackBufs& b, int rows, int block,
                 int skip_first, int32_t* out, float* logits, cudaStream_t s) {
   const dflash_config& c = m->cfg;
-  GemmParams p = gemm_base(m, rows, c.vocab, c.hidden, gemm_bn_for(rows), ws);
+  GemmParams p = gemm_base(m, rows, c.vocab, c.hidden, gemm_bn_for(rows, c.vocab, m->sms), ws);
   p.mode = EPI_ARGMAX;
   p.amax_val = b.amax_val;
   p.amax_idx = b.amax_idx;
@@ -695,6 +706,10 @@ int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflas
     // DFLASH_ATTN_TC=0 keeps the drafter on the mma.sync attention kernel
     const char* t = std::getenv("DFLASH_ATTN_TC");
     m->attn_tc = !(t != nullptr && t[0] == '0');
+    // DFLASH_TWO_TERM_LAYERS=k: two-term activations in the first k layers only
+    const char* tt = std::getenv("DFLASH_TWO_TERM_LAYERS");
+    if (tt != nullptr && tt[0] != '\0')
+      m->two_term_layers = std::max(0, std::min(m->cfg.n_layers, std::atoi(tt)));
     // DFLASH_DEP_LEAD=k: a GEMM lets the next kernel launch when its producer
     // has k weight k-blocks left to request (-1: at the start)
     const char* dl = std::getenv("DFLASH_DEP_LEAD");
@@ -802,7 +817,7 @@ int dflash_ctx_fuse(dflash_model m, const void* taps, int32_t T, void* ctx, void
   float* partial = w.take<float>(partial_floats(m, 0, T));
   float* cf = w.take<float>(static_cast<size_t>(T) * c.hidden);
   const int K = c.n_taps * c.hidden;
-  GemmParams p = gemm_base(m, T, c.hidden, K, gemm_bn_for(T), w);
+  GemmParams p = gemm_base(m, T, c.hidden, K, gemm_bn_for(T, c.hidden, m->sms), w);
   if (c.fc_norm) {
     p.mode = EPI_STORE_F32;
     p.out = cf;
@@ -835,7 +850,7 @@ int dflash_kv_append(dflash_model m, const void* ctx, const int32_t* row_req,
   float* partial = w.take<float>(partial_floats(m, 0, T));
   if (w.off > ws_bytes) return DFLASH_ERR_CAPACITY;
   for (int l = 0; l < c.n_layers; ++l) {
-    GemmParams p = gemm_base(m, T, 2 * m->kv_dim, c.hidden, gemm_bn_for(T), w);
+    GemmParams p = gemm_base(m, T, 2 * m->kv_dim, c.hidden, gemm_bn_for(T, 2 * m->kv_dim, m->sms), w);
     p.w_row0 = l * m->qkv_rows + m->q_dim;
     p.mode = EPI_QKV;
     QkvEpi e = qkv_base(m, l);

@@ -166,16 +166,33 @@ __device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int 
 template <typename Sync>
 __device__ void epi_swiglu(const GemmParams& p, const float* ts, int tile, int m0, int rows,
                            int tid, Sync sync) {
-    uint16_t* out = static_cast<uint16_t*>(p.out);
-  for (int idx = tid; idx < rows * 64; idx += 128) {
-    const int r = idx / 64, j = idx % 64;
-    const float g = ts[r * kTsLd + j];
-    const float u = ts[r * kTsLd + 64 + j];
-    const float h = silu_f(g) * u;
-    const size_t o = static_cast<size_t>(m0 + r) * p.ld_out + tile * 64 + j;
-    const uint16_t hi = f2bf(h);
-    out[o] = hi;
-    if (p.out_lo != nullptr) p.out_lo[o] = bf16_lo_part(h, hi);
+  // Thread (row r, group q of 8) forms h = silu(g) * u for pairs 4q..4q+3
+  // and 32+4q..32+4q+3 of the tile's 64: the 8 threads of a row read 128
+  // contiguous bytes per 16-byte load and store 4 bf16 at a time.
+  uint16_t* out = static_cast<uint16_t*>(p.out);
+  for (int idx = tid; idx < rows * 8; idx += 128) {
+    const int r = idx / 8, q = idx % 8;
+    const float* tr = ts + r * kTsLd;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int j = half * 32 + q * 4;
+      const float4 g = *reinterpret_cast<const float4*>(tr + j);
+      const float4 u = *reinterpret_cast<const float4*>(tr + 64 + j);
+      const float h[4] = {silu_f(g.x) * u.x, silu_f(g.y) * u.y, silu_f(g.z) * u.z, silu_f(g.w) * u.w};
+      uint16_t hi[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) hi[k] = f2bf(h[k]);
+      const size_t o = static_cast<size_t>(m0 + r) * p.ld_out + tile * 64 + j;
+      *reinterpret_cast<uint2*>(out + o) =
+          make_uint2(hi[0] | (static_cast<uint32_t>(hi[1]) << 16), hi[2] | (static_cast<uint32_t>(hi[3]) << 16));
+      if (p.out_lo != nullptr) {
+        uint16_t lo[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) lo[k] = bf16_lo_part(h[k], hi[k]);
+        *reinterpret_cast<uint2*>(p.out_lo + o) =
+            make_uint2(lo[0] | (static_cast<uint32_t>(lo[1]) << 16), lo[2] | (static_cast<uint32_t>(lo[3]) << 16));
+      }
+    }
   }
 }
 

@@ -63,9 +63,36 @@ struct GemmCfg {
   static constexpr int PRE_OFF = MAIN_BYTES + 256;
   static constexpr int PRE_BYTES = !PRE ? 0 : ((PRE_RESID || PRE_ROPE) ? 3072 : 512);
   static constexpr int PRE_RESID_ROWS = 4;
-  static constexpr int SMEM_BYTES = MAIN_BYTES + 256 + PRE_BYTES + 1024;  // + barriers, alignment slack
+  // row scales 1/rms of the m-tile's rows (deferred input RMSNorm), computed
+  // during the main loop and applied where each accumulator is last written
+  static constexpr int RINV_OFF = MAIN_BYTES + 256 + PRE_BYTES;
+  static constexpr int SMEM_BYTES = RINV_OFF + BN * 4 + 1024;  // + alignment slack
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
 };
+
+// 1/rms of rows m0 .. m0+rows-1 of the deferred input RMSNorm into out[]:
+// the row's per-tile sums of squares in one fixed order for any M
+// (accumulator i takes tiles i, i+32, ...; the 32 accumulators then combine
+// halves, quarters, ... as an xor butterfly across a warp would), 1 for rows
+// past norm_rows.  Thread t of nt takes rows t, t+nt, ...
+__device__ void row_scales(const GemmParams& p, int m0, int rows, float* out, int t, int nt) {
+  for (int r = t; r < rows; r += nt) {
+    const float* q = p.ssq_in + static_cast<size_t>(m0 + r) * p.ssq_in_tiles;
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    for (int t0 = 0; t0 < p.ssq_in_tiles; t0 += 32) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (t0 + i < p.ssq_in_tiles) acc[i] += __ldcg(q + t0 + i);
+    }
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) acc[i] += acc[i + w];
+    out[r] = (m0 + r < p.norm_rows) ? rsqrtf(acc[0] / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
+  }
+}
 
 // ---------------------------------------------------------------- kernel
 template <int BN, bool SPLIT>
@@ -194,17 +221,45 @@ __global__ void __launch_bounds__(128, 1)
   // loop) once the previous kernels' writes are visible, so that the tail
   // after the last MMA starts with them in shared memory.  Same values and
   // the same arithmetic as the epilogue's own loads.
-  float* pre_rinv = reinterpret_cast<float*>(smem + C::PRE_OFF);         // [32]
+  float* rinv_s = reinterpret_cast<float*>(smem + C::RINV_OFF);          // [BN]
   int* pre_route = reinterpret_cast<int*>(smem + C::PRE_OFF + 128);      // [3][32]
   float* pre_resid = reinterpret_cast<float*>(smem + C::PRE_OFF + 512);  // [4][128]
   float* pre_g = pre_resid + C::PRE_RESID_ROWS * kTileN;                 // [128]
   float* pre_qg = reinterpret_cast<float*>(smem + C::PRE_OFF + 512);    // [128]
   float2* pre_cs = reinterpret_cast<float2*>(smem + C::PRE_OFF + 1024);  // [4][64]
   const int rows_mt = min(BN, p.M - mt * BN);                            // rows of this m-tile
-  bool have_rinv = false, have_route = false, have_resid = false, have_rope = false;
+  bool have_route = false, have_resid = false, have_rope = false;
+  const bool rinv_early = p.ssq_in != nullptr && (p.pre_mask & 1);
   int rope_rb = 0;  // first row (in the m-tile) of the RoPE table
+  if (rinv_early && warp >= 2) {
+    if (BN <= 32) {
+      // decode-sized tiles: lane t adds tiles t, t+32, ... of rows w2, w2+2,
+      // ..., then the xor butterfly of warp_sum (the same sums as row_scales)
+      const int w2 = warp - 2;
+      float acc[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+      for (int tt = lane; tt < p.ssq_in_tiles; tt += 32) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = w2 + 2 * i;
+          if (r < rows_mt) acc[i] += __ldcg(p.ssq_in + static_cast<size_t>(m0 + r) * p.ssq_in_tiles + tt);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int r = w2 + 2 * i;
+        if (r < rows_mt) {
+          const float ss = warp_sum(acc[i]);
+          if (lane == 0)
+            rinv_s[r] = (m0 + r < p.norm_rows) ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
+        }
+      }
+    } else {
+      row_scales(p, m0, rows_mt, rinv_s, tid - 64, 64);
+    }
+  }
   if constexpr (C::PRE) {
-    have_rinv = p.ssq_in != nullptr && (p.pre_mask & 1);
     have_route = p.mode == EPI_QKV && (p.pre_mask & 2);
     if constexpr (C::PRE_ROPE) {
       // the rows this CTA will finish, as decided after the main loop
@@ -252,31 +307,6 @@ __global__ void __launch_bounds__(128, 1)
     if (warp >= 2) {
       const int w2 = warp - 2;
       const int mt0 = mt * BN;
-      if (have_rinv) {
-        // row r's sum: lane t adds tiles t, t+32, ... in order, then the xor
-        // butterfly of warp_sum (as in the epilogue below); rows w2, w2+2, ...
-        float acc[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-        for (int tt = lane; tt < p.ssq_in_tiles; tt += 32) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int r = w2 + 2 * i;
-            if (r < rows_mt) acc[i] += __ldcg(p.ssq_in + static_cast<size_t>(mt0 + r) * p.ssq_in_tiles + tt);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = w2 + 2 * i;
-          if (r < rows_mt) {
-            const float ss = warp_sum(acc[i]);
-            if (lane == 0)
-              pre_rinv[r] = (mt0 + r < p.norm_rows)
-                                ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps)
-                                : 1.f;
-          }
-        }
-      }
       if (have_route) {
         const int t = tid - 64;
         if (t < rows_mt) qkv_route(p, mt0 + t, pre_route + t, pre_route + 32 + t, pre_route + 64 + t);
@@ -314,6 +344,11 @@ __global__ void __launch_bounds__(128, 1)
   const bool aborted = *abort_flag != 0;
   tc_fence_after();
   const int rows = min(BN, p.M - m0);
+  const bool scaled = p.ssq_in != nullptr;  // rows carry the input norm's 1/rms
+  if (scaled && !rinv_early) {
+    row_scales(p, m0, rows, rinv_s, tid, 128);
+    __syncthreads();
+  }
   const int f = warp * 32 + lane;
   const int n0 = tile * kTileN;
   bool do_epi = false;
@@ -328,6 +363,17 @@ __global__ void __launch_bounds__(128, 1)
       for (int c = 0; c < BN / 16; ++c) {
         float v[16];
         tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 16, v);
+        if (scaled) {
+          // the chunk's 16 row scales, read before any of its stores
+          float sc[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 t4 = *reinterpret_cast<const float4*>(rinv_s + c * 16 + 4 * q);
+            sc[4 * q] = t4.x; sc[4 * q + 1] = t4.y; sc[4 * q + 2] = t4.z; sc[4 * q + 3] = t4.w;
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = (c * 16 + j < rows) ? v[j] * sc[j] : v[j];
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) ts[(c * 16 + j) * C::TS_LD + f] = v[j];
       }
@@ -401,8 +447,13 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int c = c0 + i * 128;
-          if (c < nchunk)
+          if (c < nchunk) {
+            if (scaled) {
+              const float sc = rinv_s[c / 32];
+              acc[i].x *= sc; acc[i].y *= sc; acc[i].z *= sc; acc[i].w *= sc;
+            }
             *reinterpret_cast<float4*>(ts + (c / 32) * C::TS_LD + (c % 32) * 4) = acc[i];
+          }
         }
       }
       if (tid == 0) p.counters[mt * n_tiles + tile] = 0;
@@ -454,6 +505,10 @@ __global__ void __launch_bounds__(128, 1)
           const float4 v = recv[(sp * rpc + lr) * 32 + c4];
           acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
         }
+        if (scaled) {
+          const float sc = rinv_s[r_beg + lr];
+          acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+        }
         *reinterpret_cast<float4*>(ts + (r_beg + lr) * C::TS_LD + c4 * 4) = acc;
       }
       __syncthreads();
@@ -490,8 +545,13 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int c = c0 + i * 128;
-          if (c < nchunk)
+          if (c < nchunk) {
+            if (scaled) {
+              const float sc = rinv_s[r_beg + c / 32];
+              red[i].x *= sc; red[i].y *= sc; red[i].z *= sc; red[i].w *= sc;
+            }
             *reinterpret_cast<float4*>(ts + (r_beg + c / 32) * C::TS_LD + (c % 32) * 4) = red[i];
+          }
         }
       }
       __syncthreads();
@@ -501,49 +561,6 @@ __global__ void __launch_bounds__(128, 1)
   float* tsv = ts + r_beg * C::TS_LD;   // first row this CTA finishes
   const int m0v = m0 + r_beg;
   const int rows_v = r_cnt;
-  if (do_epi && p.ssq_in != nullptr) {
-    // Sum of the row's per-tile sums in one fixed order for any M: lane t of
-    // a warp accumulates tiles t, t+32, ... and the 32 lane sums combine as
-    // the xor butterfly of warp_sum.  Up to 32 rows: one warp per row.  More
-    // rows: one thread per row computes the same sums with all of the row's
-    // loads in flight (a warp per row would wait one load round trip per row).
-    float* rinv = reinterpret_cast<float*>(smem + C::SCRATCH_OFF);
-    if (have_rinv) {
-      rinv = pre_rinv + r_beg;  // computed during the main loop
-    } else if (rows_v <= 32) {
-      for (int r = warp; r < rows_v; r += 4) {
-        const float* q = p.ssq_in + static_cast<size_t>(m0v + r) * p.ssq_in_tiles;
-        float ss = 0.f;
-        for (int t = lane; t < p.ssq_in_tiles; t += 32) ss += __ldcg(q + t);
-        ss = warp_sum(ss);
-        if (lane == 0)
-          rinv[r] = (m0v + r < p.norm_rows) ? rsqrtf(ss / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
-      }
-    } else {
-      for (int r = tid; r < rows_v; r += 128) {
-        const float* q = p.ssq_in + static_cast<size_t>(m0v + r) * p.ssq_in_tiles;
-        float acc[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) acc[t] = 0.f;
-        for (int t0 = 0; t0 < p.ssq_in_tiles; t0 += 32) {
-#pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (t0 + t < p.ssq_in_tiles) acc[t] += __ldcg(q + t0 + t);
-        }
-#pragma unroll
-        for (int w = 16; w > 0; w >>= 1)
-#pragma unroll
-          for (int t = 0; t < w; ++t) acc[t] += acc[t + w];
-        rinv[r] = (m0v + r < p.norm_rows) ? rsqrtf(acc[0] / static_cast<float>(p.norm_dim) + p.norm_eps) : 1.f;
-      }
-    }
-    __syncthreads();
-    for (int idx = tid; idx < rows_v * kTileN; idx += 128) {
-      const int r = idx / kTileN, f = idx % kTileN;
-      tsv[r * C::TS_LD + f] *= rinv[r];
-    }
-    __syncthreads();
-  }
   if (do_epi) {
     CtaSync sync;
     switch (p.mode) {
@@ -594,8 +611,11 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ---------------------------------------------------------------- host side
-int gemm_bn_for(int M) {
-  return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+int gemm_bn_for(int M, int N, int sms) {
+  if (M <= 128) return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  // more rows: 256-row tiles, or 128-row tiles where 256-row tiles would
+  // leave SMs without a tile (fewer output tiles than SMs)
+  return (N / kTileN) * ((M + 255) / 256) < sms ? 128 : 256;
 }
 
 template <bool SPLIT>

@@ -115,8 +115,9 @@ struct GemmParams {
                          // routing, 4 residual rows, 8 QKV gains and RoPE tables
 };
 
-// Picks the MMA N width for M rows and the split-K count.
-int gemm_bn_for(int M);
+// MMA N width (activation rows per tile) for M rows and N output features
+// on a device with `sms` SMs.
+int gemm_bn_for(int M, int N, int sms);
 int gemm_max_smem_bytes();
 // Clusters of `cluster` CTAs (BN variant) that can be resident at once.
 int gemm_max_active_clusters(int bn, int cluster);

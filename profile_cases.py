@@ -8,7 +8,8 @@
 lm_head: the shared LM head + argmax of the Qwen3-8B-shaped drafter
 (151936 x 4096 bf16 weights, `rows` rows), launched a few times, ~1.7 GB on
 the device.  step: a few eager draft steps of a workload (default
-qwen3_8b_b1; --kv e4m3: E4M3 context cache; --batch: fewer requests).  target: block-verify passes of the end-to-end workload's
+qwen3_8b_b1; --kv e4m3: E4M3 context cache; --batch: fewer requests; --ctx: context
+length).  target: block-verify passes of the end-to-end workload's
 8-layer H=4096 target (batch 8 x 16 rows, context 1024), ~5 GB.  sampling:
 draft sampling and the temperature-1 verify at batch 32, block 16, vocab
 151936 (random logits, ~0.7 GB).
@@ -46,12 +47,14 @@ def lm_head(iters=3, rows=16):
     print("lm_head ok", out[:4].tolist())
 
 
-def step(config="qwen3_8b_b1", iters=3, kv="bf16", batch=None):
+def step(config="qwen3_8b_b1", iters=3, kv="bf16", batch=None, ctx=None):
     from dataclasses import replace
     from block_diffusion_speculative_fuse_gb300.session import DraftStep
     wl = W.get_workload(config)
     if batch is not None:
         wl = replace(wl, batch=batch)
+    if ctx is not None:
+        wl = replace(wl, ctx_len=ctx)
     st = DraftStep(wl, kv_dtype=kv)
     torch.cuda.synchronize()
     torch.cuda.empty_cache()  # the bf16 staging of an E4M3 cache
@@ -104,6 +107,7 @@ def main():
     ap.add_argument("--rows", type=int, default=16)
     ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"])
     ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--ctx", type=int, default=None, help="context length per request")
     a = ap.parse_args()
     _build.build()
     B.load()
@@ -114,7 +118,7 @@ def main():
     elif a.case == "sampling":
         sampling(a.iters)
     else:
-        step(a.config, a.iters, a.kv, a.batch)
+        step(a.config, a.iters, a.kv, a.batch, a.ctx)
 
 
 if __name__ == "__main__":
