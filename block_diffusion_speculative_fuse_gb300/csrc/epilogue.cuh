@@ -14,7 +14,10 @@ constexpr int kTsLd = kTileN + 4;  // staged tile row stride (floats)
 // sin/cos of pos * inv_freq with inv_freq held as an unevaluated float pair
 // (hi + lo).  The product is formed exactly with an FMA (Dekker's two-product)
 // and reduced modulo 2*pi with a three-piece Cody-Waite split of 2*pi, so the
-// reduced angle is accurate to ~1e-6 rad for positions up to 2^24.
+// reduced angle is accurate to ~1e-6 rad for positions up to 2^24; its sine
+// and cosine come from the hardware approximation, whose absolute error on
+// [-pi, pi] (below 2^-21.4, per NVIDIA's documentation of __sincosf) is
+// smaller than the angle's.
 __device__ __forceinline__ void rope_sincos(int pos, float2 f, float* s, float* c) {
   const float pf = static_cast<float>(pos);
   const float a_hi = pf * f.x;
@@ -30,7 +33,7 @@ __device__ __forceinline__ void rope_sincos(int pos, float2 f, float* s, float* 
   r = fmaf(-k, P2, r);
   r = fmaf(-k, P3, r);
   r += a_lo;
-  sincosf(r, s, c);
+  __sincosf(r, s, c);
 }
 
 // ---------------------------------------------------------------- argmax keys
@@ -67,21 +70,26 @@ __device__ void epi_store(const GemmParams& p, const float* ts, int tile, int m0
 
 // pre_resid (nullable): the residual rows m0 .. m0+rows-1 of this tile's 128
 // columns, already loaded ([rows][128]); pre_g (nullable): gnext of the tile.
+// x_new = x + acc, then the optional depthwise conv along block positions
+// (sliding window down each column, zero padded at each request's block
+// edges), then the outputs: x_new (fp32), the next norm's input
+// bf16(x_new * gnext) (+ its low term), bf16(x_new) for taps, and the row's
+// sum of squares over the tile.
 template <typename Sync>
 __device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int rows,
                           int tid, Sync sync, const float* pre_resid = nullptr,
                           const float* pre_g = nullptr) {
-    // Thread f owns feature column n0 + f: x_new = x + acc, then the optional
-  // depthwise conv along block positions (sliding window down the column,
-  // zero padded at each request's block edges), then the next norm's inputs.
-  const int f = tid;
-  const int n = tile * kTileN + f;
+  const int warp = tid / 32, lane = tid % 32;
+  const int n0 = tile * kTileN;
+  const bool conv = p.conv != nullptr && p.conv_width > 0;
+  bool added = false;  // residual already in ts
   if (pre_resid != nullptr) {
-    for (int r = 0; r < rows; ++r) ts[r * kTsLd + f] += pre_resid[r * kTileN + f];
-  } else {
-    // the tile's residual rows as 16-byte pieces, 16 loads in flight per
-    // thread, added where they land (then every column is complete)
-    const float* rbase = p.resid + static_cast<size_t>(m0) * p.ld_resid + tile * kTileN;
+    for (int r = 0; r < rows; ++r) ts[r * kTsLd + tid] += pre_resid[r * kTileN + tid];
+    added = true;
+  } else if (conv) {
+    // the conv needs whole columns: the tile's residual rows as 16-byte
+    // pieces first, 16 loads in flight per thread, added where they land
+    const float* rbase = p.resid + static_cast<size_t>(m0) * p.ld_resid + n0;
     const int pieces = rows * (kTileN / 4);
     for (int c0 = tid; c0 < pieces; c0 += 128 * 16) {
       float4 v[16];
@@ -102,9 +110,13 @@ __device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int 
         }
       }
     }
-    sync();
+    added = true;
   }
-  if (p.conv != nullptr && p.conv_width > 0) {
+  if (conv) {
+    sync();
+    // thread f slides the window down feature column n0 + f
+    const int f = tid;
+    const int n = n0 + f;
     const int c = (p.conv_width - 1) / 2;
     float w[7];
 #pragma unroll
@@ -125,40 +137,70 @@ __device__ void epi_resid(const GemmParams& p, float* ts, int tile, int m0, int 
 #pragma unroll
         for (int j = 0; j < 6; ++j) win[j] = win[j + 1];
         const int nxt = i + 1 + c;
-        if (p.conv_width > 0) {
-          const float v = (nxt < p.block) ? ts[(r0 + nxt) * kTsLd + f] : 0.f;
-          // window length is conv_width; keep the slot after the last live one
-          win[p.conv_width - 1] = v;
-        }
+        const float v = (nxt < p.block) ? ts[(r0 + nxt) * kTsLd + f] : 0.f;
+        win[p.conv_width - 1] = v;  // window length is conv_width
         ts[(r0 + i) * kTsLd + f] = y;
       }
     }
   }
-  const float gn = p.xg_out == nullptr ? 0.f : (pre_g != nullptr ? pre_g[f] : bf2f(p.gnext[n]));
-  for (int r = 0; r < rows; ++r) {
-    const float x = ts[r * kTsLd + f];
-    const size_t m = static_cast<size_t>(m0 + r);
-    p.resid[m * p.ld_resid + n] = x;
-    if (p.xg_out != nullptr) {
-      const float xg = x * gn;
-      const uint16_t hi = f2bf(xg);
-      p.xg_out[m * p.ld_xg + n] = hi;
-      if (p.xg_lo != nullptr) p.xg_lo[m * p.ld_xg + n] = bf16_lo_part(xg, hi);
-    }
-    if (p.raw_out != nullptr) p.raw_out[m * p.ld_raw + n] = f2bf(x);
-  }
-  if (p.ssq_out != nullptr) {
-    sync();
-    const int warp = tid / 32, lane = tid % 32;
-    for (int r = warp; r < rows; r += 4) {
-      float ss = 0.f;
+  sync();  // every column complete before the row-wise output pass
+  // Outputs: warp w takes rows w*4 .. w*4+3 of every 16, lane l columns
+  // 4l .. 4l+3 (16-byte fp32 and 8-byte bf16 stores; the row's sum of
+  // squares is the warp sum of the lanes' 4-term sums).
+  float gn[4] = {0.f, 0.f, 0.f, 0.f};
+  if (p.xg_out != nullptr) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float v = ts[r * kTsLd + lane + 32 * k];
-        ss = fmaf(v, v, ss);
+    for (int k = 0; k < 4; ++k) gn[k] = pre_g != nullptr ? pre_g[4 * lane + k] : bf2f(p.gnext[n0 + 4 * lane + k]);
+  }
+  for (int r0 = warp * 4; r0 < rows; r0 += 16) {
+    float4 res[4];
+    if (!added) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        res[i] = r0 + i < rows ? __ldcg(reinterpret_cast<const float4*>(
+                                     p.resid + static_cast<size_t>(m0 + r0 + i) * p.ld_resid + n0) + lane)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = r0 + i;
+      if (r >= rows) break;  // warp-uniform
+      float4 x = *reinterpret_cast<const float4*>(ts + r * kTsLd + 4 * lane);
+      if (!added) {
+        x.x += res[i].x; x.y += res[i].y; x.z += res[i].z; x.w += res[i].w;
       }
-      ss = warp_sum(ss);
-      if (lane == 0) p.ssq_out[static_cast<size_t>(m0 + r) * p.ssq_ld + tile] = ss;
+      const size_t m = static_cast<size_t>(m0 + r);
+      *reinterpret_cast<float4*>(p.resid + m * p.ld_resid + n0 + 4 * lane) = x;
+      const float xv[4] = {x.x, x.y, x.z, x.w};
+      if (p.xg_out != nullptr) {
+        uint16_t hi[4], lo[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float xg = xv[k] * gn[k];
+          hi[k] = f2bf(xg);
+          lo[k] = bf16_lo_part(xg, hi[k]);
+        }
+        const size_t o = m * p.ld_xg + n0 + 4 * lane;
+        *reinterpret_cast<uint2*>(p.xg_out + o) =
+            make_uint2(hi[0] | (static_cast<uint32_t>(hi[1]) << 16), hi[2] | (static_cast<uint32_t>(hi[3]) << 16));
+        if (p.xg_lo != nullptr)
+          *reinterpret_cast<uint2*>(p.xg_lo + o) =
+              make_uint2(lo[0] | (static_cast<uint32_t>(lo[1]) << 16), lo[2] | (static_cast<uint32_t>(lo[3]) << 16));
+      }
+      if (p.raw_out != nullptr) {
+        const size_t o = m * p.ld_raw + n0 + 4 * lane;
+        *reinterpret_cast<uint2*>(p.raw_out + o) =
+            make_uint2(f2bf(xv[0]) | (static_cast<uint32_t>(f2bf(xv[1])) << 16),
+                       f2bf(xv[2]) | (static_cast<uint32_t>(f2bf(xv[3])) << 16));
+      }
+      if (p.ssq_out != nullptr) {
+        float ss = xv[0] * xv[0];
+        ss = fmaf(xv[1], xv[1], ss);
+        ss = fmaf(xv[2], xv[2], ss);
+        ss = fmaf(xv[3], xv[3], ss);
+        ss = warp_sum(ss);
+        if (lane == 0) p.ssq_out[m * p.ssq_ld + tile] = ss;
+      }
     }
   }
 }
