@@ -390,6 +390,31 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
   const int items = rows * per_tile;
   // The loop bound depends on the warp only, so every lane reaches the
   // shuffles; items past the end or skipped rows only drop their stores.
+  // The next iteration's tile values and routing are read before this
+  // iteration's global stores (loads are not moved across those stores), so
+  // their latency overlaps this iteration's arithmetic.
+  float nx1[8], nx2[8];
+  int nreq = 0, npos = 0, npg = 0;
+  auto fetch = [&](int w0n) {
+    const int wn = w0n + grp;
+    const bool in = wn < items;
+    const int rn = in ? wn / per_tile : 0, hln = in ? wn % per_tile : 0;
+    nreq = r_req[rn];
+    npos = r_pos[rn];
+    npg = r_pg[rn];
+    const float* xs = ts + rn * kTsLd + hln * d + c0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (4 * q < P) {
+        a = *reinterpret_cast<const float4*>(xs + 4 * q);
+        b = *reinterpret_cast<const float4*>(xs + half + 4 * q);
+      }
+      nx1[4 * q] = a.x; nx1[4 * q + 1] = a.y; nx1[4 * q + 2] = a.z; nx1[4 * q + 3] = a.w;
+      nx2[4 * q] = b.x; nx2[4 * q + 1] = b.y; nx2[4 * q + 2] = b.z; nx2[4 * q + 3] = b.w;
+    }
+  };
+  if (warp * 4 < items) fetch(warp * 4);
   for (int w0 = warp * 4; w0 < items; w0 += 16) {
     const int w = w0 + grp;
     bool act = w < items;
@@ -399,20 +424,15 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
     const int kind = head < hq ? 0 : (head < hq + hkv ? 1 : 2);
     const int hidx = kind == 0 ? head : (kind == 1 ? head - hq : head - hq - hkv);
     const bool is_blk = m < e.n_blk;
-    const int req = r_req[r], pos = r_pos[r], pg = r_pg[r];
-    if (!is_blk && (pg == -2 || (kind == 0 && !e.keep_q_pool))) act = false;
-    const float* xs = ts + r * kTsLd + hl * d + c0;
+    const int req = nreq, pos = npos, pg = npg;
     float x1[8], x2[8];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-      if (4 * q < P) {
-        a = *reinterpret_cast<const float4*>(xs + 4 * q);
-        b = *reinterpret_cast<const float4*>(xs + half + 4 * q);
-      }
-      x1[4 * q] = a.x; x1[4 * q + 1] = a.y; x1[4 * q + 2] = a.z; x1[4 * q + 3] = a.w;
-      x2[4 * q] = b.x; x2[4 * q + 1] = b.y; x2[4 * q + 2] = b.z; x2[4 * q + 3] = b.w;
+    for (int j = 0; j < 8; ++j) {
+      x1[j] = nx1[j];
+      x2[j] = nx2[j];
     }
+    if (w0 + 16 < items) fetch(w0 + 16);
+    if (!is_blk && (pg == -2 || (kind == 0 && !e.keep_q_pool))) act = false;
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) ss += x1[j] * x1[j] + x2[j] * x2[j];  // zero past P
@@ -451,12 +471,14 @@ __device__ void epi_qkv(const GemmParams& p, const float* ts, int tile, int m0, 
     // E4M3 context cache: amax of the head vector's bf16 values over its 8
     // lanes (every lane takes part in the shuffles)
     float am = 0.f;
+    if (e.pool8 != nullptr) {  // uniform over the kernel
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < P) am = fmaxf(am, fmaxf(fabsf(bf2f(f2bf(x1[j]))), fabsf(bf2f(f2bf(x2[j])))));
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      for (int j = 0; j < 8; ++j)
+        if (j < P) am = fmaxf(am, fmaxf(fabsf(bf2f(f2bf(x1[j]))), fabsf(bf2f(f2bf(x2[j])))));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    }
     if (!act) continue;
     if (kind > 0 && !is_blk && e.pool8 != nullptr) {
       const float scale = am > 0.f ? am / 448.f : 1.f;
