@@ -529,7 +529,8 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
       uint32_t sr0[32], sr1[32];
       tmem_ld32_nowait(lane_base + C::S_COL0 + b * kChunkKeys, sr0);
       tmem_ld32_nowait(lane_base + C::S_COL0 + b * kChunkKeys + 32, sr1);
-      tmem_wait_ld();
+      tmem_wait_ld(sr0);
+      tmem_regs_ready(sr1);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[b]);
@@ -601,12 +602,12 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
         for (int q = 0; q < D / 32; ++q) {
           uint32_t o[32];
           tmem_ld32_nowait(lane_base + C::O_COL + q * 32, o);
-          tmem_wait_ld();
+          tmem_wait_ld(o);
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
           tmem_st32(lane_base + C::O_COL + q * 32, o);
+          tmem_wait_st();  // before o is reloaded
         }
-        tmem_wait_st();
         l_sum *= alpha;
       }
       if (raise_m) m_used = mc;
@@ -704,7 +705,7 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
       uint32_t o[32];
       if (have) {
         tmem_ld32_nowait(lane_base + C::O_COL + q * 32, o);
-        tmem_wait_ld();
+        tmem_wait_ld(o);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = 0u;
@@ -742,7 +743,7 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
       uint32_t o[32];
       if (have) {
         tmem_ld32_nowait(lane_base + C::O_COL + q * 32, o);
-        tmem_wait_ld();
+        tmem_wait_ld(o);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = 0u;

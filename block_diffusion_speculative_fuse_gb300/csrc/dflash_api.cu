@@ -125,7 +125,7 @@ const uint16_t* u16(const void* p) { return static_cast<const uint16_t*>(p); }
 // only, never on the number of activation rows.
 int choose_splits(const dflash_model_s* m, int n_tiles, int m_tiles, int kb_total, int bn) {
   // resident CTAs per SM of the GEMM (shared-memory bound): 3 for BN <= 32
-  const int per_sm = bn <= 32 ? 3 : bn <= 64 ? 2 : 1;
+  const int per_sm = bn <= 32 ? 3 : bn <= 128 ? 2 : 1;
   const int capacity = m->sms * (m->is_draft ? per_sm : 2);
   const int base = n_tiles * (m->is_draft ? m_tiles : 1);
   int s = capacity / std::max(1, base);

@@ -33,10 +33,11 @@ struct GemmCfg {
   // slots the next kernel's CTAs (programmatic dependent launch) occupy the
   // third and prefetch their first weight stages.  A split activation operand
   // (hi + lo tiles) enlarges a stage, so those variants keep fewer stages.
-  // (two-term BN = 128: 2 stages of 48 KB, so two CTAs fit per SM)
+  // (BN = 128: 3 stages of 32 KB, or 2 of 48 KB two-term, so two CTAs fit
+  // per SM and each SM runs eight warps of epilogue)
   static constexpr int STAGES =
       SPLIT ? (BN <= 64 ? 3 : 2)
-            : (BN <= 16 ? 4 : BN <= 32 ? 3 : BN <= 64 ? 4 : BN <= 128 ? 6 : 4);
+            : (BN <= 16 ? 4 : BN <= 32 ? 3 : BN <= 64 ? 4 : BN <= 128 ? 3 : 4);
   static constexpr int A_BYTES = kTileN * kTileK * 2;  // 16 KB
   static constexpr int B_BYTES = BN * kTileK * 2;      // one activation tile
   static constexpr int B_STAGE = SPLIT ? 2 * B_BYTES : B_BYTES;
@@ -379,6 +380,8 @@ __global__ void __launch_bounds__(128, 1)
       }
       do_epi = true;
     }
+    // thread f staged feature column f; the epilogues read across columns
+    __syncthreads();
   } else if (!p.cluster) {
     // Split-K through global memory: every CTA stores its fp32 partial tile;
     // the last CTA of the tile (atomic ticket, no waiting) sums the partials

@@ -91,3 +91,35 @@ def test_e2e_8layer_shapes_spec_equals_ar_and_oracle():
     sure = (top[:, -1] - top[:, -2]) > 0.1
     assert sure.sum() > 0
     assert np.array_equal(toks[sure], np.argmax(lref, -1)[sure])
+
+
+@pytest.mark.parametrize("batch", [8, 16])
+def test_e2e_8layer_block_verify_equals_one_token_decode(batch):
+    """Batch invariance of the target at the end-to-end shapes with the
+    activation tiles a batch-8/16 verify pass uses (16 block rows per
+    request: 128/256 rows, the 128- and 256-row GEMM tiles) against
+    one-token decode (8/16 rows, 16-row tiles): after the same prefill, one
+    verify pass over 16 tokens per request gives the logits of 16 single-
+    token decode passes bit for bit."""
+    from block_diffusion_speculative_fuse_gb300.device import DeviceModel, i32
+    from block_diffusion_speculative_fuse_gb300.generate import TargetRunner
+    wl = W.get_workload("e2e_8layer")
+    ts = wl.target
+    shared = W.shared_weights(ts, wl.wid)
+    tm = DeviceModel(ts, W.target_weights(ts, wl.wid), shared, draft=False)
+    V, n, Pp = ts.vocab, 16, 80
+    prompt = W.uniform_tokens(batch * Pp, V, wl.wid, W.TENSOR_IDS["prompt"], 21).reshape(batch, Pp)
+    toks = W.uniform_tokens(batch * n, V, wl.wid, W.TENSOR_IDS["prompt"], 22).reshape(batch, n)
+    blk = TargetRunner(tm, batch, Pp + n + 1, Pp)
+    blk.forward(i32(prompt), i32([0] * batch), Pp)
+    lb = torch.zeros((batch * n, V), dtype=torch.float32, device="cuda")
+    blk.forward(i32(toks), i32([Pp] * batch), n, logits=lb)
+    one = TargetRunner(tm, batch, Pp + n + 1, Pp)
+    one.forward(i32(prompt), i32([0] * batch), Pp)
+    l1 = torch.zeros((batch, V), dtype=torch.float32, device="cuda")
+    lb = lb.view(batch, n, V)
+    for i in range(n):
+        one.forward(i32(toks[:, i:i + 1]), i32([Pp + i] * batch), 1, logits=l1)
+        torch.cuda.synchronize()
+        diff = (l1 != lb[:, i]).sum().item()
+        assert diff == 0, f"position {i}: {diff} logits differ"
