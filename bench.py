@@ -368,10 +368,7 @@ def run_ours(args, rank, world, dist):
     e1.synchronize()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
     clocks = sampler.stop() if rank == 0 else None
 
     status = st.status()
@@ -414,7 +411,7 @@ def run_ours(args, rank, world, dist):
                 h.copy_(dv, non_blocking=True)
         e3.record(stream)
     e3.synchronize()
-    ms_e2e = e2.elapsed_time(e3) / ke
+    ms_e2e = max_over_ranks(e2.elapsed_time(e3) / ke, dist)
 
     # dominant kernel: the LM-head GEMM (+ its argmax reduce), timed alone
     rows = wl.batch * d.block
@@ -443,8 +440,8 @@ def run_ours(args, rank, world, dist):
     sb = step_bytes(wl, st.ctx_before, st.new_rows, args.kv)
     sf = step_flops(wl, st.ctx_before, st.new_rows)
     steps_per_s = 1e3 / ms
-    drafted = steps_per_s * wl.batch * (d.block - 1) * world
-    accepted = steps_per_s * emitted_per_step * world
+    drafted = whole_job_rate(wl.batch * (d.block - 1), ms, world)
+    accepted = whole_job_rate(emitted_per_step, ms, world)
     lmb = lm_head_bytes(d, rows)
     lm_gbs = lmb / (ms_lm * 1e-3) / 1e9
     traffic = profiled_traffic(wl.name)
@@ -471,7 +468,7 @@ def run_ours(args, rank, world, dist):
                      "achieved": lm_gbs, "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm,
                      "traffic": traffic, "bytes_per_launch": lmb, "ms_per_launch": ms_lm,
                      "peak_kind": pk_kind},
-        "e2e": {"value": 1e3 / ms_e2e * wl.batch * (d.block - 1) * world,
+        "e2e": {"value": whole_job_rate(wl.batch * (d.block - 1), ms_e2e, world),
                 "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": ms_e2e},
         "gpu_launches": int(launches_per_step * args.steps),
@@ -572,10 +569,39 @@ def run_e2e(args, rank, world):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ ranks
+def check_world(gpus, world):
+    """--gpus must name the number of ranks the launcher started (one per
+    GPU); N > 1 is launched through torch.distributed.run."""
+    if gpus != world:
+        raise SystemExit(f"--gpus {gpus} but {world} rank(s) were launched: run "
+                         f"`python -m torch.distributed.run --nproc-per-node {gpus} bench.py "
+                         f"--gpus {gpus} ...` (or omit --gpus for one GPU)")
+
+
+def max_over_ranks(x, dist):
+    """The largest value of x over all ranks (the job's time is its slowest
+    rank's): an all-reduce on the GPU under NCCL, on the host under gloo."""
+    if dist is None:
+        return x
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step, ms_max, world):
+    """Units per second of the whole job: every rank processes the same
+    per-step work (weak scaling), timed by the slowest rank's step."""
+    return units_per_rank_step * world * 1e3 / ms_max
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    check_world(args.gpus, world)
     dist = None
     if world > 1:
         import torch
