@@ -10,10 +10,15 @@
 // k with a * S < C_k (C_k the running sum of the weights, S their total).
 //
 // Arithmetic: row maxima in fp32 (exact), exponentials of (z - max) / T in
-// fp32, every sum and running sum in fp64 in a fixed order; the accept test
-// evaluates its two probabilities with fp64 exp.  Against an all-fp64
-// evaluation a decision can therefore differ only when its uniform lies
-// within about 1e-6 (relative) of a boundary.
+// fp32; the row statistics and the draws from a softmax (draft sampling,
+// the bonus token) add each thread's exponentials in fp32 with Kahan
+// compensation and combine the thread sums in fp64 (the GPU's fp64 rate is
+// low, and a plain fp64 sum per element set the pace); the residual draw
+// max(0, p - q) sums in fp64 (its terms cancel); every running sum over the
+// threads is fp64, in a fixed order; the accept test evaluates its two
+// probabilities with fp64 exp.  Against an all-fp64 evaluation a decision
+// can therefore differ only when its uniform lies within about 1e-6
+// (relative) of a boundary.
 //
 // Kernels:
 //   sample_stats_kernel   one CTA per logits row: (max, S) of the row
@@ -133,6 +138,46 @@ __device__ int draw_inverse_cdf(int V, double a, WFn wfn, double* red, int* foun
   return k;
 }
 
+// The same draw for weights given in fp32 by wfn(k) >= 0 with no
+// cancellation in them (exponentials): each thread's segment sum in fp32
+// with Kahan compensation, the scan of the segment sums and the walk in
+// fp64.  The walk adds the same terms in fp64, so a target within a few fp32
+// ulps of a segment's end can fall past its last element; the draw then
+// returns that element.
+template <typename WFn>
+__device__ int draw_inverse_cdf_f32(int V, double a, WFn wfn, double* red, int* found) {
+  const int seg = (V + kSampThreads - 1) / kSampThreads;
+  const int k0 = threadIdx.x * seg, k1 = min(V, k0 + seg);
+  float s = 0.f, comp = 0.f;
+  for (int k = k0; k < k1; ++k) {
+    const float y = wfn(k) - comp;
+    const float t = s + y;
+    comp = (t - s) - y;
+    s = t;
+  }
+  const double sd = static_cast<double>(s) - static_cast<double>(comp);
+  double S = 0.0;
+  const double pre = block_exclusive_scan_f64(sd, red, &S);
+  const double target = a * S;
+  if (threadIdx.x == 0) *found = V - 1;
+  __syncthreads();
+  if (k0 < k1 && pre <= target && target < pre + sd) {
+    double c = pre;
+    int k = k1 - 1;
+    for (int j = k0; j < k1; ++j) {
+      c += static_cast<double>(wfn(j));
+      if (target < c) {
+        k = j;
+        break;
+      }
+    }
+    atomicMin(found, k);
+  }
+  __syncthreads();
+  const int k = *found;
+  __syncthreads();
+  return k;
+}
 // Row rr of a blocked logits array [.][block][V] whose first `skip` rows of
 // every block are not used: block rr / (block - skip), row skip + rr % (...).
 __device__ __forceinline__ const float* blocked_row(const float* base, int rr, int block, int skip,
@@ -155,13 +200,42 @@ __global__ void __launch_bounds__(kSampThreads)
   if (r >= nq + np) return;
   const float* z = r < nq ? blocked_row(q_rows, r, q_block, q_skip, V)
                           : p_rows + static_cast<size_t>(r - nq) * V;
+  const bool vec = V % 4 == 0 && (reinterpret_cast<uintptr_t>(z) & 15) == 0;
+  const float4* z4 = reinterpret_cast<const float4*>(z);
   float mx = -INFINITY;
-  for (int k = threadIdx.x; k < V; k += kSampThreads) mx = fmaxf(mx, __ldg(z + k));
+  if (vec) {
+    for (int k = threadIdx.x; k < V / 4; k += kSampThreads) {
+      const float4 v = __ldg(z4 + k);
+      mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+    }
+  } else {
+    for (int k = threadIdx.x; k < V; k += kSampThreads) mx = fmaxf(mx, __ldg(z + k));
+  }
   mx = block_max_f32(mx, redf);
-  double s = 0.0;
-  for (int k = threadIdx.x; k < V; k += kSampThreads) s += static_cast<double>(expf((__ldg(z + k) - mx) / T));
-  s = block_sum_f64(s, redd);
-  if (threadIdx.x == 0) stats[r] = make_double2(static_cast<double>(mx), s);
+  // Each thread adds its exponentials in fp32 with a compensation term
+  // (Kahan): the lost low parts are carried, so the thread's sum is within
+  // a few fp32 ulps of the exact sum of its terms; the thread sums are then
+  // added in fp64 in a fixed order.
+  float s = 0.f, comp = 0.f;
+  auto add = [&](float x) {
+    const float y = expf((x - mx) / T) - comp;
+    const float t = s + y;
+    comp = (t - s) - y;
+    s = t;
+  };
+  if (vec) {
+    for (int k = threadIdx.x; k < V / 4; k += kSampThreads) {
+      const float4 v = __ldg(z4 + k);
+      add(v.x);
+      add(v.y);
+      add(v.z);
+      add(v.w);
+    }
+  } else {
+    for (int k = threadIdx.x; k < V; k += kSampThreads) add(__ldg(z + k));
+  }
+  const double S = block_sum_f64(static_cast<double>(s) - static_cast<double>(comp), redd);
+  if (threadIdx.x == 0) stats[r] = make_double2(static_cast<double>(mx), S);
 }
 
 // Probability of token k in a row with stats (max, S), in fp64.
@@ -226,9 +300,8 @@ __global__ void __launch_bounds__(kSampThreads)
       return pk > qk ? pk - qk : 0.0;
     }, red, &found);
   } else {
-    tok = draw_inverse_cdf(V, a, [&](int k) {
-      return static_cast<double>(expf((__ldg(prow + k) - mp) / T));
-    }, red, &found);
+    tok = draw_inverse_cdf_f32(V, a, [&](int k) { return expf((__ldg(prow + k) - mp) / T); }, red,
+                               &found);
   }
   if (threadIdx.x < B) {
     const int j = threadIdx.x;
@@ -257,9 +330,8 @@ __global__ void __launch_bounds__(kSampThreads)
   const int r = blockIdx.x;
   const float* z = blocked_row(rows, r, block, skip, V);
   const float m = static_cast<float>(stats[r].x);
-  const int k = draw_inverse_cdf(V, a[r], [&](int j) {
-    return static_cast<double>(expf((__ldg(z + j) - m) / T));
-  }, red, &found);
+  const int k = draw_inverse_cdf_f32(V, a[r], [&](int j) { return expf((__ldg(z + j) - m) / T); },
+                                     red, &found);
   if (threadIdx.x == 0) out[r] = k;
 }
 
