@@ -123,3 +123,31 @@ def test_e2e_8layer_block_verify_equals_one_token_decode(batch):
         torch.cuda.synchronize()
         diff = (l1 != lb[:, i]).sum().item()
         assert diff == 0, f"position {i}: {diff} logits differ"
+
+
+def test_e2e_8layer_decode_step_repeats_bit_for_bit():
+    """One-token decode of the 8-layer H=4096 target repeated 2000 times from
+    the same state (batch 8 after a 1300-token prefill; each repeat rewrites
+    the same cache slot with the same values) gives the same logits every
+    time.  A race between threads of a kernel (a missing barrier, a register
+    read before its asynchronous load) shows up here as rare differences."""
+    from block_diffusion_speculative_fuse_gb300.device import DeviceModel, i32
+    from block_diffusion_speculative_fuse_gb300.generate import TargetRunner
+    wl = W.get_workload("e2e_8layer")
+    ts = wl.target
+    tm = DeviceModel(ts, W.target_weights(ts, wl.wid), W.shared_weights(ts, wl.wid), draft=False)
+    b, P, reps = 8, 1300, 2000
+    prompts = W.uniform_tokens(b * P, ts.vocab, wl.wid, W.TENSOR_IDS["prompt"], 31).reshape(b, P)
+    run = TargetRunner(tm, b, P + 64, P)
+    run.forward(i32(prompts), i32([0] * b), P)
+    tok = i32(W.uniform_tokens(b, ts.vocab, wl.wid, W.TENSOR_IDS["prompt"], 32).reshape(b, 1))
+    pos = i32([P] * b)
+    ref = torch.zeros((b, ts.vocab), dtype=torch.float32, device="cuda")
+    lg = torch.zeros_like(ref)
+    run.forward(tok, pos, 1, logits=ref)
+    bad = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for _ in range(reps):
+        run.forward(tok, pos, 1, logits=lg)
+        bad += (lg != ref).any().long()
+    torch.cuda.synchronize()
+    assert bad.item() == 0, f"{bad.item()} of {reps} repeats differ"
