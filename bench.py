@@ -90,6 +90,29 @@ def step_flops(wl, ctx_before, new_rows):
     return dense + attn
 
 
+def phase_roofline(wl, ctx_before, new_rows, kv, hbm_gbs, tc_tflops):
+    """Lower bound on the step time as a sum over its two kinds of phase,
+    each at max(bytes / HBM bandwidth, flops / tensor rate): attention
+    (context K/V read once per layer, QK^T and PV flops) and the GEMMs
+    (every other algorithmic byte, the dense flops).  Equals the HBM-only
+    bound when both phases are bandwidth-bound (batch 1, DFlash-2); larger
+    when the GEMMs are tensor-bound (batch 32)."""
+    d = wl.draft
+    kv_b = 2.0 if kv == "bf16" else 1.0 + 4.0 / d.head_dim
+    L_after = np.asarray(ctx_before) + np.asarray(new_rows)
+    attn_bytes = kv_b * int(L_after.sum()) * 2 * d.kv_dim * d.n_layers
+    keys = np.asarray(ctx_before) + np.asarray(new_rows) + d.block
+    attn_flops = d.n_layers * 4 * d.block * d.n_q_heads * d.head_dim * int(keys.sum())
+    total_bytes = step_bytes(wl, ctx_before, new_rows, kv)
+    gemm_bytes = total_bytes - attn_bytes
+    gemm_flops = step_flops(wl, ctx_before, new_rows) - attn_flops
+    t_attn = max(attn_bytes / (hbm_gbs * 1e9), attn_flops / (tc_tflops * 1e12))
+    t_gemm = max(gemm_bytes / (hbm_gbs * 1e9), gemm_flops / (tc_tflops * 1e12))
+    return {"t_min_ms": (t_attn + t_gemm) * 1e3, "attention_ms": t_attn * 1e3, "gemm_ms": t_gemm * 1e3,
+            "gemm_bound": "tensor" if gemm_flops / (tc_tflops * 1e12) > gemm_bytes / (hbm_gbs * 1e9)
+            else "hbm"}
+
+
 def acceptance_profile(hist, p):
     """Per-position acceptance from hist[n] = number of (request, step)
     samples that accepted n drafts (n = 0..B-1).  Block position i (1-based)
@@ -438,6 +461,9 @@ def run_ours(args, rank, world, dist):
     pk, pk_kind = peaks()
     hbm = float(pk["hbm_gbs"])
     sb = step_bytes(wl, st.ctx_before, st.new_rows, args.kv)
+    # a step's kernels run back to back for a long time: the sustained rate
+    tc = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", 1700.0)))
+    phase = phase_roofline(wl, st.ctx_before, st.new_rows, args.kv, hbm, tc)
     sf = step_flops(wl, st.ctx_before, st.new_rows)
     steps_per_s = 1e3 / ms
     drafted = whole_job_rate(wl.batch * (d.block - 1), ms, world)
@@ -464,6 +490,8 @@ def run_ours(args, rank, world, dist):
         "step_roofline": {"bound": "hbm", "bytes": sb, "flops": sf, "achieved": step_gbs,
                           "peak": hbm, "unit": "GB/s", "frac": step_gbs / hbm,
                           "peak_kind": pk_kind},
+        "phase_roofline": dict(phase, frac=phase["t_min_ms"] / ms, tensor_peak_tflops=tc,
+                               bound="mixed" if phase["gemm_bound"] == "tensor" else "hbm"),
         "roofline": {"bound": "hbm", "kernel": "gemm_tc05 LM head + argmax (151936x4096)",
                      "achieved": lm_gbs, "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm,
                      "traffic": traffic, "bytes_per_launch": lmb, "ms_per_launch": ms_lm,

@@ -49,3 +49,24 @@ def test_step_bytes_of_the_batch1_step():
     assert d.n_layers == 5 and d.hidden == 4096
     assert abs(b - approx) / approx < 1e-3
     assert abs(b - 3.385e9) / 3.385e9 < 1e-3
+
+
+def test_phase_roofline_reduces_to_hbm_at_batch_1_and_is_mixed_at_batch_32():
+    hbm, tc = 6689.5, 1693.4
+    for name, bound in (("qwen3_8b_b1", "hbm"), ("qwen3_8b_b32_paged", "tensor")):
+        wl = W.get_workload(name)
+        ctx, new = W.ctx_lengths(wl), W.new_row_counts(wl)
+        ph = bench.phase_roofline(wl, ctx, new, "bf16", hbm, tc)
+        hbm_ms = bench.step_bytes(wl, ctx, new) / (hbm * 1e9) * 1e3
+        flop_ms = bench.step_flops(wl, ctx, new) / (tc * 1e12) * 1e3
+        assert ph["gemm_bound"] == bound
+        assert abs(ph["t_min_ms"] - (ph["attention_ms"] + ph["gemm_ms"])) < 1e-12
+        # never below either whole-step bound, never above their sum
+        assert ph["t_min_ms"] >= max(hbm_ms, flop_ms) - 1e-9
+        assert ph["t_min_ms"] <= hbm_ms + flop_ms + 1e-9
+        if bound == "hbm":
+            assert abs(ph["t_min_ms"] - hbm_ms) < 1e-9
+    # batch 32: ~1.48 ms (the survey's estimate for this workload is ~1.4 ms)
+    wl = W.get_workload("qwen3_8b_b32_paged")
+    ph = bench.phase_roofline(wl, W.ctx_lengths(wl), W.new_row_counts(wl), "bf16", hbm, tc)
+    assert 1.3 < ph["t_min_ms"] < 1.6
