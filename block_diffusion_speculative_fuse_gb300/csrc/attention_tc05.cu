@@ -9,10 +9,14 @@
 //
 // Query rows: the G = hq/hkv query heads that share the KV head times the n
 // block rows, row index i*G + h (R = n*G rows).  Keys are streamed in chunks
-// of 64 (four 16-key pages) by TMA, one box per (page, K|V, 64-column half),
-// into a 4-deep ring of 128-byte-swizzled stages; pages past the split or
-// missing from the table are read from beyond the end of the tensor map,
-// which fills them with zeros.
+// of 64 (four 16-key pages) by TMA into a 4-deep ring of 128-byte-swizzled
+// stages.  A K plane is laid out [64-column half][64 keys][128 B] (the S MMA
+// reads all 64 keys of a column slice at once), filled by one box per (page,
+// half); a V plane [page][half][16 keys][128 B] (the PV MMA reads one page
+// per instruction), filled by one box per page.  The SM's TMA unit spends a
+// roughly fixed time per box, so fewer, larger boxes keep it ahead of HBM.
+// Pages past the split or missing from the table are read from beyond the
+// end of the tensor map, which fills them with zeros.
 //
 // Per chunk c (warp 5 lane 0 issues, fp32 accumulators in TMEM):
 //   S[c%2] = Q K^T            M = 128 rows, N = 64 keys, K = head_dim
@@ -65,10 +69,13 @@ struct TcCfg {
   static constexpr int HALVES = D / 64;
   static constexpr int Q_BYTES = 128 * D * 2;                   // [HALVES][128 rows][64]
   static constexpr int P_BYTES = 128 * kChunkKeys * 2;          // [128 rows][64 keys]
-  static constexpr int KV_HALF = kChunkKeys * 64 * 2;           // [64 keys][64 cols] = 8 KB
-  static constexpr int K_BYTES = kChunkKeys * D * 2;            // [HALVES][64][64]
+  static constexpr int KV_HALF = kChunkKeys * 64 * 2;           // K plane: [64 keys][64 cols] = 8 KB
+  static constexpr int K_BYTES = kChunkKeys * D * 2;            // one plane (K: [HALVES][64][64])
+  static constexpr int PH_BYTES = 16 * 128;                     // V plane: 16 keys of one half
+  static constexpr int PPL_BYTES = HALVES * PH_BYTES;           // V plane: one page [HALVES][16][64]
   static constexpr int STAGE_BYTES = PLANES * K_BYTES;          // K, V (, K_lo, V_lo)
-  static constexpr int BOXES = kChunkPages * PLANES * HALVES;   // TMA boxes per chunk
+  static constexpr int K_BOXES = kChunkPages * TERMS * HALVES;  // TMA boxes per chunk: K planes
+  static constexpr int BOXES = K_BOXES + kChunkPages * TERMS;   // + one per page and V plane
   static constexpr int Q_OFF = 0;
   static constexpr int P_OFF = Q_OFF + Q_BYTES;
   static constexpr int KV_OFF = P_OFF + 2 * P_BYTES;
@@ -115,6 +122,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int D, bool CAUSAL = false, int TERMS = 1, bool FP8 = false>
 __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
     attn_tc05_kernel(const __grid_constant__ CUtensorMap pool_map,
+                     const __grid_constant__ CUtensorMap pool_v_map,
                      const __grid_constant__ CUtensorMap kblk_map,
                      const __grid_constant__ CUtensorMap vblk_map,
                      const __grid_constant__ AttnTcParams p) {
@@ -168,6 +176,7 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&pool_map);
+    if (!FP8) tma_prefetch_desc(&pool_v_map);
     tma_prefetch_desc(&kblk_map);
     tma_prefetch_desc(&vblk_map);
   }
@@ -316,7 +325,10 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
     const int t = tid - 192;
     const int c8 = t % CH, r0 = t / CH;
     const uint32_t f8_base = smem_u32(sm + C::F8_OFF) + r0 * D + c8 * 8;
-    const uint32_t b16_base = smem_u32(sm + C::KV_OFF) + r0 * 128 + (c8 / 8) * C::KV_HALF +
+    // row phase r0 % 8 = key % 8 for every key this thread writes (RPP % 8 == 0)
+    const uint32_t k16_base = smem_u32(sm + C::KV_OFF) + r0 * 128 + (c8 / 8) * C::KV_HALF +
+                              (((c8 % 8) ^ (r0 % 8)) << 4);
+    const uint32_t v16_base = smem_u32(sm + C::KV_OFF + C::K_BYTES) + (c8 / 8) * C::PH_BYTES +
                               (((c8 % 8) ^ (r0 % 8)) << 4);
     int done_c = 0;
     for (int c = 0; c < nch; ++c) {
@@ -341,16 +353,17 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
           for (int pp = 0; pp < kChunkPages; ++pp) {
             if (idv[pp] > -2) continue;
             const int y = (req * p.hkv + g) * p.n + (-2 - idv[pp]) * 16;
-            for (int kv = 0; kv < 2; ++kv)
-              for (int hf = 0; hf < C::HALVES; ++hf)
-                tma_load_2d(sm + C::KV_OFF + sb * C::STAGE_BYTES + kv * C::K_BYTES + hf * C::KV_HALF +
-                                pp * 16 * 128,
-                            kv ? &vblk_map : &kblk_map, hf * 64, y, &kv_full[sb], pol);
+            uint8_t* kd = sm + C::KV_OFF + sb * C::STAGE_BYTES + pp * 16 * 128;
+            for (int hf = 0; hf < C::HALVES; ++hf)
+              tma_load_2d(kd + hf * C::KV_HALF, &kblk_map, hf * 64, y, &kv_full[sb], pol);
+            tma_load_3d(sm + C::KV_OFF + sb * C::STAGE_BYTES + C::K_BYTES + pp * C::PPL_BYTES,
+                        &vblk_map, 0, y, 0, &kv_full[sb], pol);
           }
         }
       }
       const uint32_t src = f8_base + st8 * C::F8_STAGE_BYTES;
-      const uint32_t dst = b16_base + sb * C::STAGE_BYTES;
+      const uint32_t kdst = k16_base + sb * C::STAGE_BYTES;
+      const uint32_t vdst = v16_base + sb * C::STAGE_BYTES;
 #pragma unroll
       for (int j0 = 0; j0 < 2 * JPK; j0 += 8) {
         uint2 cd[8];
@@ -374,7 +387,7 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
             o = make_uint4(e4m3x2_to_bf16x2(cd[u].x), e4m3x2_to_bf16x2(cd[u].x >> 16),
                            e4m3x2_to_bf16x2(cd[u].y), e4m3x2_to_bf16x2(cd[u].y >> 16));
           }
-          st_shared_u4(dst + kv * C::K_BYTES + RPP * i * 128, o);
+          st_shared_u4(kv ? vdst + pp * C::PPL_BYTES + (key % 16) * 128 : kdst + RPP * i * 128, o);
         }
       }
       if (t < 2 * kChunkKeys) {
@@ -421,23 +434,33 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if (lane < C::BOXES) {
-        // lane -> (page, plane, 64-column half); planes K, V (, K_lo, V_lo)
-        const int pp = lane / (C::PLANES * C::HALVES), kv = (lane / C::HALVES) % C::PLANES,
-                  hf = lane % C::HALVES;
+        // lanes [0, K_BOXES): (page, K term, 64-column half), one 2-D box each;
+        // then (page, V term): both halves of the page's V rows in one 3-D box.
+        // Planes of a pool page: K, V (, K_lo, V_lo).
+        const bool kb = lane < C::K_BOXES;
+        const int j = kb ? lane : lane - C::K_BOXES;
+        const int pp = kb ? j / (TERMS * C::HALVES) : j / TERMS;
+        const int t = kb ? (j / C::HALVES) % TERMS : j % TERMS;
+        const int hf = kb ? j % C::HALVES : 0;
+        const int kv = 2 * t + (kb ? 0 : 1);
         const int id = pages_s[c * kChunkPages + pp];
-        const CUtensorMap* map = &pool_map;
+        bool blk = false;
         int y;
         if (id >= 0) {
           y = p.pool_row0 + ((id * C::PLANES + kv) * p.hkv + g) * 16;
         } else if (id <= -2) {
-          map = kv ? &vblk_map : &kblk_map;
+          blk = true;
           y = (req * p.hkv + g) * p.n + (-2 - id) * 16;
         } else {
           y = p.pool_rows;  // past the end: zero fill
         }
-        uint8_t* dst = sm + C::KV_OFF + st * C::STAGE_BYTES + kv * C::K_BYTES + hf * C::KV_HALF +
-                       pp * 16 * 128;
-        tma_load_2d(dst, map, hf * 64, y, &kv_full[st], pol);
+        uint8_t* dst = sm + C::KV_OFF + st * C::STAGE_BYTES + kv * C::K_BYTES;
+        if (kb)
+          tma_load_2d(dst + hf * C::KV_HALF + pp * 16 * 128, blk ? &kblk_map : &pool_map, hf * 64, y,
+                      &kv_full[st], pol);
+        else
+          tma_load_3d(dst + pp * C::PPL_BYTES, blk ? &vblk_map : &pool_v_map, 0, y, 0, &kv_full[st],
+                      pol);
       }
       ++issued;
       if (c == min(nch, kStages) - 1) griddep_launch_dependents();
@@ -487,8 +510,8 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < kChunkKeys / 16; ++k) {
             const uint64_t ad = umma_desc_sw128(p_addr + k * 32);
-            // keys 16k..16k+15 = rows of the V tile; d halves are C::KV_HALF apart
-            const uint64_t bd = umma_desc_sw128_mn(vt + k * 16 * 128, C::KV_HALF, 1024);
+            // keys 16k..16k+15 = page k of the V plane; its d halves are C::PH_BYTES apart
+            const uint64_t bd = umma_desc_sw128_mn(vt + k * C::PPL_BYTES, C::PH_BYTES, 1024);
             umma_bf16(tmem + C::O_COL, ad, bd, idesc_pv, (c > 0 || t > 0 || k > 0) ? 1u : 0u);
           }
         }
@@ -656,10 +679,9 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
           const int key = idx / (C::HALVES * 8), rem = idx % (C::HALVES * 8);
           const int hf = rem / 8, c16 = rem % 8;
           if ((key % 16) >= cntp[key / 16]) {
-            *reinterpret_cast<uint4*>(vst + hf * C::KV_HALF + swz128(key, c16)) = make_uint4(0u, 0u, 0u, 0u);
-            if (TERMS == 2)
-              *reinterpret_cast<uint4*>(vst + 2 * C::K_BYTES + hf * C::KV_HALF + swz128(key, c16)) =
-                  make_uint4(0u, 0u, 0u, 0u);
+            uint8_t* v16 = vst + (key / 16) * C::PPL_BYTES + hf * C::PH_BYTES + swz128(key % 16, c16);
+            *reinterpret_cast<uint4*>(v16) = make_uint4(0u, 0u, 0u, 0u);
+            if (TERMS == 2) *reinterpret_cast<uint4*>(v16 + 2 * C::K_BYTES) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
       }
@@ -825,7 +847,8 @@ __global__ void __launch_bounds__(TcCfg<D, TERMS, FP8>::THREADS, 1)
 }
 
 template <int D, bool CAUSAL, int TERMS, bool FP8 = false>
-cudaError_t launch_tc(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
+cudaError_t launch_tc(const CUtensorMap* pool_map, const CUtensorMap* pool_v_map,
+                      const CUtensorMap* kblk_map,
                       const CUtensorMap* vblk_map, const AttnTcParams& p, cudaStream_t s,
                       bool pdl) {
   using C = TcCfg<D, TERMS, FP8>;
@@ -861,8 +884,8 @@ cudaError_t launch_tc(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
   cfg.attrs = attrs;
   cfg.numAttrs = na;
   count_launch();
-  return cudaLaunchKernelEx(&cfg, attn_tc05_kernel<D, CAUSAL, TERMS, FP8>, *pool_map, *kblk_map,
-                            *vblk_map, p);
+  return cudaLaunchKernelEx(&cfg, attn_tc05_kernel<D, CAUSAL, TERMS, FP8>, *pool_map, *pool_v_map,
+                            *kblk_map, *vblk_map, p);
 }
 
 }  // namespace
@@ -935,32 +958,32 @@ bool attention_tc_ok(int d, int hq, int hkv, int n, int page_size, int split_pag
          n * (hq / hkv) <= 128 && split_pages <= kMaxPagesTc;
 }
 
-cudaError_t attention_tc_launch(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
-                                const CUtensorMap* vblk_map, const AttnTcParams& p,
-                                cudaStream_t s, bool pdl) {
+cudaError_t attention_tc_launch(const CUtensorMap* pool_map, const CUtensorMap* pool_v_map,
+                                const CUtensorMap* kblk_map, const CUtensorMap* vblk_map,
+                                const AttnTcParams& p, cudaStream_t s, bool pdl) {
   if (p.n_splits < 1 || p.n_splits > kMaxAttnCluster) return cudaErrorInvalidValue;
   if (p.rows_per_tile < 1 || p.rows_per_tile * (p.hq / p.hkv) > 128) return cudaErrorInvalidValue;
   if (p.causal) {
     // the target path: dual-state query tiles only, one- or two-term K/V
     if (p.rows_per_tile * (p.hq / p.hkv) > 64) return cudaErrorInvalidValue;
     if (p.kv_terms == 2) {
-      if (p.d == 128) return launch_tc<128, true, 2>(pool_map, kblk_map, vblk_map, p, s, pdl);
-      if (p.d == 64) return launch_tc<64, true, 2>(pool_map, kblk_map, vblk_map, p, s, pdl);
+      if (p.d == 128) return launch_tc<128, true, 2>(pool_map, pool_v_map, kblk_map, vblk_map, p, s, pdl);
+      if (p.d == 64) return launch_tc<64, true, 2>(pool_map, pool_v_map, kblk_map, vblk_map, p, s, pdl);
     } else {
-      if (p.d == 128) return launch_tc<128, true, 1>(pool_map, kblk_map, vblk_map, p, s, pdl);
-      if (p.d == 64) return launch_tc<64, true, 1>(pool_map, kblk_map, vblk_map, p, s, pdl);
+      if (p.d == 128) return launch_tc<128, true, 1>(pool_map, pool_v_map, kblk_map, vblk_map, p, s, pdl);
+      if (p.d == 64) return launch_tc<64, true, 1>(pool_map, pool_v_map, kblk_map, vblk_map, p, s, pdl);
     }
     return cudaErrorInvalidValue;
   }
   if (p.kv_terms == 2) return cudaErrorInvalidValue;
   if (p.fp8) {
     if (p.scales == nullptr) return cudaErrorInvalidValue;
-    if (p.d == 128) return launch_tc<128, false, 1, true>(pool_map, kblk_map, vblk_map, p, s, pdl);
-    if (p.d == 64) return launch_tc<64, false, 1, true>(pool_map, kblk_map, vblk_map, p, s, pdl);
+    if (p.d == 128) return launch_tc<128, false, 1, true>(pool_map, pool_v_map, kblk_map, vblk_map, p, s, pdl);
+    if (p.d == 64) return launch_tc<64, false, 1, true>(pool_map, pool_v_map, kblk_map, vblk_map, p, s, pdl);
     return cudaErrorInvalidValue;
   }
-  if (p.d == 128) return launch_tc<128, false, 1>(pool_map, kblk_map, vblk_map, p, s, pdl);
-  if (p.d == 64) return launch_tc<64, false, 1>(pool_map, kblk_map, vblk_map, p, s, pdl);
+  if (p.d == 128) return launch_tc<128, false, 1>(pool_map, pool_v_map, kblk_map, vblk_map, p, s, pdl);
+  if (p.d == 64) return launch_tc<64, false, 1>(pool_map, pool_v_map, kblk_map, vblk_map, p, s, pdl);
   return cudaErrorInvalidValue;
 }
 

@@ -65,6 +65,23 @@ int encode_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ERR_INVALID_ARG;
 }
 
+// 3-D bf16 map over [rows][d] (d = 64 or 128): dims (64 columns, row, d/64
+// column halves), box (64, 16, d/64): 16 rows of both column halves as
+// [half][16 rows][128 B], 128-byte swizzled, zero fill out of bounds.
+int encode_map_rows16(CUtensorMap* map, const void* base, uint64_t rows, uint32_t d) {
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (d != 64 && d != 128))
+    return DFLASH_ERR_INVALID_ARG;
+  cuuint64_t dims[3] = {64, rows, d / 64};
+  cuuint64_t strides[2] = {d * 2ull, 128ull};
+  cuuint32_t box[3] = {64, 16, d / 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ERR_INVALID_ARG;
+}
+
 // 2-D uint8 map over [rows][cols] bytes (cols a multiple of 16), box
 // [box_rows][cols], no swizzle, zero fill out of bounds.
 int encode_map_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
@@ -423,7 +440,9 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
   const int tc_splits = plan.splits;
   const bool fp8 = kv->dtype == 1;
   if (fp8 && !use_tc) return DFLASH_ERR_UNSUPPORTED;  // E4M3 caches: tcgen05 attention only
-  CUtensorMap pool_map, kblk_map, vblk_map;
+  // K pages as 2-D boxes (one per 64-column half), V pages as 3-D boxes
+  // (both halves of a page in one box); E4M3 pools: one uint8 map of codes
+  CUtensorMap pool_map, pool_v_map, kblk_map, vblk_map;
   if (use_tc) {
     int rc = fp8 ? encode_map_u8(&pool_map, kv->pool, pool_rows, c.head_dim, 16)
                  : encode_map(&pool_map, kv->pool, pool_rows, c.head_dim, c.head_dim, 16);
@@ -431,8 +450,12 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       rc = encode_map(&kblk_map, b.kblk, static_cast<uint64_t>(rows) * c.n_kv_heads, c.head_dim,
                       c.head_dim, 16);
     if (!rc)
-      rc = encode_map(&vblk_map, b.vblk, static_cast<uint64_t>(rows) * c.n_kv_heads, c.head_dim,
-                      c.head_dim, 16);
+      rc = encode_map_rows16(&vblk_map, b.vblk, static_cast<uint64_t>(rows) * c.n_kv_heads,
+                             c.head_dim);
+    if (!rc)
+      rc = fp8 ? encode_map_rows16(&pool_v_map, b.vblk,
+                                   static_cast<uint64_t>(rows) * c.n_kv_heads, c.head_dim)
+               : encode_map_rows16(&pool_v_map, kv->pool, pool_rows, c.head_dim);
     if (rc) return rc;
   }
   // Two-term (hi + lo bf16) activations for O, gate/up and down.  The
@@ -502,7 +525,7 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
       a.out = b.o;
       a.out_lo = two ? b.o_lo : nullptr;
       a.status = ws.status();
-      DF_CUDA(attention_tc_launch(&pool_map, &kblk_map, &vblk_map, a, s, true));
+      DF_CUDA(attention_tc_launch(&pool_map, &pool_v_map, &kblk_map, &vblk_map, a, s, true));
     } else {
       AttnParams a;
       std::memset(&a, 0, sizeof(a));

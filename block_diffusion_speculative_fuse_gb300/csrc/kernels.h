@@ -175,9 +175,12 @@ struct AttnTcParams {
   uint16_t* out_lo;      // optional low halves
   int32_t* status;
 };
-cudaError_t attention_tc_launch(const CUtensorMap* pool_map, const CUtensorMap* kblk_map,
-                                const CUtensorMap* vblk_map, const AttnTcParams& p,
-                                cudaStream_t s, bool pdl);
+// pool_map: 2-D, box 16 rows x 64 columns (bf16) or 16 rows x d bytes
+// (E4M3 codes); pool_v_map, vblk_map: 3-D, box 16 rows x both column halves
+// (pool_v_map unused by E4M3 caches); kblk_map: 2-D like pool_map.
+cudaError_t attention_tc_launch(const CUtensorMap* pool_map, const CUtensorMap* pool_v_map,
+                                const CUtensorMap* kblk_map, const CUtensorMap* vblk_map,
+                                const AttnTcParams& p, cudaStream_t s, bool pdl);
 // Pages per key split for `pairs` (request, KV head) pairs over
 // `total_pages` 16-key pages (context pages + block pages).
 int attention_tc_split_pages(int d, int pairs, int total_pages);
