@@ -14,10 +14,13 @@ CPU ``rms_norm``, ``scaled_dot_product_attention``, ``linear``, ``silu``) or
 brute force; the composed draft step is pinned by invariants (non-causality,
 context-order invariance, RoPE shift invariance, incremental == one-shot
 context projection, DFlash-2 conv reductions) and the speculative loop by
-token identity with autoregressive greedy decoding.  Parity unpinned: the
-numerical values of a full random-init draft step have no external
-reference (there is no trained model and no printed example); only the
-pinned pieces and invariants above vouch for them.
+token identity with autoregressive greedy decoding; the composition of the
+layer stacks (tests/test_oracle_layer_pins.py) by special cases with closed
+forms: zero output/down projections (identity layers), equal values
+(attention returns V whatever the scores) and the DFlash-2 convolution
+against PyTorch's conv1d, with planted mistakes that must fail.  A full
+random-init step has no external reference value (no trained model, no
+printed example); the pins above vouch for every piece of it.
 
 ``oracle.sampling`` holds the sampling-mode (temperature > 0) verify: the
 standard speculative-sampling acceptance rule applied to a block draft,

@@ -24,22 +24,28 @@ def built():
     binding.load()
 
 
-def models(wl, target_std=0.02):
+def models(wl, target_std=0.02, distinct_gains=False):
     from block_diffusion_speculative_fuse_gb300.device import DeviceModel
     ts, ds = wl.target, wl.draft
     shared = W.shared_weights(ts, wl.wid, std=target_std)
     tw = W.target_weights(ts, wl.wid, std=target_std)
     dw = W.draft_weights(ds, wl.wid)
+    if distinct_gains:
+        tw = W.jittered_gains(tw, wl.wid + 1)
+        dw = W.jittered_gains(dw, wl.wid + 2)
     tm = DeviceModel(ts, tw, shared, draft=False)
     dm = DeviceModel(ds, dw, {k: tm.t[k] for k in ("embed", "lm_head")}, draft=True)
     return shared, tw, dw, tm, dm
 
 
-def test_target_forward_parity_and_taps_tiny():
+@pytest.mark.parametrize("distinct_gains", [False, True])
+def test_target_forward_parity_and_taps_tiny(distinct_gains):
+    """distinct_gains: every RMSNorm of the target with its own non-unit
+    gains (a kernel reading the wrong gain vector fails)."""
     from block_diffusion_speculative_fuse_gb300.device import i32
     from block_diffusion_speculative_fuse_gb300.generate import TargetRunner
     wl = W.get_workload("tiny_e2e")
-    shared, tw, dw, tm, dm = models(wl, target_std=0.05)
+    shared, tw, dw, tm, dm = models(wl, target_std=0.05, distinct_gains=distinct_gains)
     P = 40
     prompt = W.uniform_tokens(P, wl.target.vocab, wl.wid, W.TENSOR_IDS["prompt"])
     run = TargetRunner(tm, 1, 128, P, wl.tap_layers)

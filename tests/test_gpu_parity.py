@@ -185,9 +185,9 @@ def draft_reference(st, d, dws, r, c_rows, o):
     return O.draft_block(d, dws, int(h["anchor"][r]), C + T, ks, vs, return_hidden=True)
 
 
-def check_draft_step(wl):
+def check_draft_step(wl, weights=None):
     from block_diffusion_speculative_fuse_gb300.session import DraftStep
-    st = DraftStep(wl, keep_host=True)
+    st = DraftStep(wl, keep_host=True, weights=weights)
     d = wl.draft
     rows = st.batch * st.B
     logits = torch.zeros((rows, d.vocab), dtype=torch.float32, device="cuda")
@@ -231,6 +231,22 @@ def test_draft_block_parity_small(kw):
     wl = tiny_workload("draft", wid=750 + kw["hidden"] + kw["batch"] + kw["block"], mlp=512,
                        vocab=2048, n_layers=2, n_taps=3, ctx_len_range=(1, 300), **kw)
     check_draft_step(wl)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, block=8, batch=3),
+    dict(hidden=512, n_q_heads=4, n_kv_heads=1, head_dim=128, block=16, batch=2, conv_width=3),
+    dict(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=128, block=16, batch=16),
+])
+def test_draft_block_parity_distinct_norm_gains(kw):
+    """Every RMSNorm (fuse, attention input, q/k, MLP input, final) with its
+    own non-unit gains, so that a kernel reading the wrong gain vector (or
+    none) fails.  The last case has 256 block rows: 128-row GEMM tiles and
+    one-term activations past the first two layers."""
+    wid = 900 + kw["hidden"] + kw["batch"]
+    wl = tiny_workload("gains", wid=wid, mlp=256, vocab=1024, n_layers=3, n_taps=3,
+                       ctx_len_range=(1, 400), **kw)
+    check_draft_step(wl, weights=W.jittered_gains(W.draft_weights(wl.draft, wid), wid))
 
 
 def test_draft_block_long_context_many_splits():

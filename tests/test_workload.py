@@ -84,3 +84,20 @@ def test_splitmix64_published_sequence():
         out = [int(v) for v in G.splitmix64_np(z)]
     assert out == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F,
                    0xF88BB8A8724C81EC]
+
+
+def test_jittered_gains_replace_only_the_norm_gains():
+    d = tiny_workload("gains", wid=5, conv_width=3).draft
+    w = W.draft_weights(d, 5)
+    j = W.jittered_gains(w, 5)
+    j2 = W.jittered_gains(w, 5)
+    for k in w:
+        if k in W.GAIN_KEYS:
+            assert j[k].shape == w[k].shape and j[k].dtype == np.uint16
+            assert np.array_equal(j[k], j2[k])                      # seeded
+            g = (j[k].astype(np.uint32) << 16).view(np.float32)
+            assert 0.5 < g.mean() < 1.5 and g.std() > 0.1           # not ones
+        else:
+            assert j[k] is w[k]
+    gains = [j[k].ravel()[:64] for k in W.GAIN_KEYS if k in j]
+    assert len({g.tobytes() for g in gains}) == len(gains)          # distinct per tensor

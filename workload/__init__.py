@@ -15,10 +15,12 @@ from .shapes import (ModelShape, DraftShape, Workload, WORKLOADS, get_workload,
 from .gen import (bf16_bits, normal_bf16, ones_bf16, uniform_tokens, rng_for,
                   draft_weights, target_weights, shared_weights, taps_bf16,
                   context_kv_bf16, page_table, ctx_lengths, agreement_probs,
-                  synth_target_ids, new_row_counts, agree_threshold, TENSOR_IDS)
+                  synth_target_ids, new_row_counts, agree_threshold, TENSOR_IDS,
+                  jittered_gains, GAIN_KEYS)
 
 __all__ = [
     "ModelShape", "DraftShape", "Workload", "WORKLOADS", "get_workload",
+    "jittered_gains", "GAIN_KEYS",
     "tiny_workload", "bf16_bits", "normal_bf16", "ones_bf16", "uniform_tokens",
     "rng_for", "draft_weights", "target_weights", "shared_weights",
     "taps_bf16", "context_kv_bf16", "page_table", "ctx_lengths",

@@ -23,7 +23,7 @@ TENSOR_IDS = {
     "post_norm": 15, "w_gate_up": 16, "w_down": 17, "conv": 18,
     "taps": 200, "ctx_k": 201, "ctx_v": 202, "anchor": 203, "prompt": 204,
     "ctx_len": 205, "agree_p": 206, "page_perm": 207, "prev_accept": 208,
-    "synth_seed": 209, "block_x": 210,
+    "synth_seed": 209, "block_x": 210, "gain_jitter": 220,
 }
 TARGET_OFFSET = 100   # target-model tensors use TENSOR_IDS[name] + 100
 
@@ -122,6 +122,23 @@ def draft_weights(d: DraftShape, wid: int, std: float = 0.02,
         w["conv"] = normal_bf16((d.n_layers, H, d.conv_width), conv_std, wid,
                                 TENSOR_IDS["conv"])
     return w
+
+
+GAIN_KEYS = ("in_norm", "post_norm", "q_norm", "k_norm", "final_norm", "fc_norm")
+
+
+def jittered_gains(weights: dict, wid: int, std: float = 0.25) -> dict:
+    """A copy of a weight dict whose RMSNorm gains are bf16(1 + std*N(0, 1))
+    instead of ones, every gain tensor from its own stream: with distinct
+    gains, reading the wrong gain vector changes the result."""
+    out = dict(weights)
+    for i, k in enumerate(GAIN_KEYS):
+        if k in weights:
+            g = rng_for(wid, TENSOR_IDS["gain_jitter"] + i)
+            x = np.float32(1.0) + np.float32(std) * g.standard_normal(weights[k].shape,
+                                                                      dtype=np.float32)
+            out[k] = bf16_bits(x)
+    return out
 
 
 def target_weights(m: ModelShape, wid: int, std: float = 0.02):
