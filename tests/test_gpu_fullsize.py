@@ -3,8 +3,10 @@
 
 qwen3_8b_b1: the whole step against the oracle (every logit of the block,
 the final hidden rows, the drafts, the verify outputs).
-qwen3_8b_b32_paged and dflash2_b16: sampled requests (first and last of the
-batch) against the oracle, which computes a request's block independently.
+qwen3_8b_b32_paged and dflash2_b16: sampled requests (the first, the last,
+and one from the middle of the batch: for the ragged batch the request with
+the longest context, whose keys span the most splits) against the oracle,
+which computes a request's block independently.
 """
 import numpy as np
 import pytest
@@ -63,11 +65,13 @@ def oracle_request(st, d, dws, c_rows, r):
     return O.draft_block(d, dws, int(h["anchor"][r]), C + T, ks, vs, return_hidden=True)
 
 
-def check_requests(name, requests):
+def check_requests(name, requests, longest=False):
     from block_diffusion_speculative_fuse_gb300.session import DraftStep
     wl = W.get_workload(name)
     d = wl.draft
     st = DraftStep(wl, keep_host=True)
+    if longest:
+        requests = sorted(set(requests) | {int(np.argmax(st.anchor_pos_np))})
     rows = st.batch * st.B
     logits = torch.zeros((rows, d.vocab), dtype=torch.float32, device="cuda")
     hidden = torch.zeros((rows, d.hidden), dtype=torch.float32, device="cuda")
@@ -117,8 +121,8 @@ def test_qwen3_8b_b1_full_step():
 
 
 def test_qwen3_8b_b32_paged_sampled_requests():
-    check_requests("qwen3_8b_b32_paged", [0, 31])
+    check_requests("qwen3_8b_b32_paged", [0, 31], longest=True)
 
 
 def test_dflash2_b16_sampled_requests():
-    check_requests("dflash2_b16", [0, 15])
+    check_requests("dflash2_b16", [0, 7, 15])
