@@ -66,8 +66,8 @@ def test_phase_roofline_reduces_to_hbm_at_batch_1_and_is_mixed_at_batch_32():
         assert ph["t_min_ms"] <= hbm_ms + flop_ms + 1e-9
         if bound == "hbm":
             assert abs(ph["t_min_ms"] - hbm_ms) < 1e-9
-    # batch 32: ~1.48 ms (attention ~0.9 ms at HBM speed, the 512-row GEMMs
-    # ~0.6 ms at the sustained tensor rate)
+    # batch 32: ~1.48 ms (attention ~0.47 ms at HBM speed, the 512-row GEMMs
+    # ~1.0 ms at the sustained tensor rate)
     wl = W.get_workload("qwen3_8b_b32_paged")
     ph = bench.phase_roofline(wl, W.ctx_lengths(wl), W.new_row_counts(wl), "bf16", hbm, tc)
     assert 1.3 < ph["t_min_ms"] < 1.6
