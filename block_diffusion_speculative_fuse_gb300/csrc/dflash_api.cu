@@ -452,10 +452,12 @@ int run_stack(const dflash_model_s* m, Ws& ws, StackBufs& b, int batch, int n,
     if (!rc)
       rc = encode_map_rows16(&vblk_map, b.vblk, static_cast<uint64_t>(rows) * c.n_kv_heads,
                              c.head_dim);
-    if (!rc)
-      rc = fp8 ? encode_map_rows16(&pool_v_map, b.vblk,
-                                   static_cast<uint64_t>(rows) * c.n_kv_heads, c.head_dim)
-               : encode_map_rows16(&pool_v_map, kv->pool, pool_rows, c.head_dim);
+    if (!rc) {
+      if (fp8)
+        pool_v_map = vblk_map;  // unused: the E4M3 kernel reads V codes through pool_map
+      else
+        rc = encode_map_rows16(&pool_v_map, kv->pool, pool_rows, c.head_dim);
+    }
     if (rc) return rc;
   }
   // Two-term (hi + lo bf16) activations for O, gate/up and down.  The
